@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark of the ROCmFP2 decode GEMV (the headline workload) on GB300.
+
+Workload: ROCmFP2 weights [M=14336, K=4096] (Student-t(5) x 0.02 with 1% of
+columns x8, seed 1), fp32 activations ~ N(0,1); one step = one rfp2_gemv call
+(fused Q8_1 activation quantize + GEMV) on batch 1.  The metric is packed
+weight bytes per second (18,350,080 bytes per call).
+
+Timing: W warm-up steps, then exactly K steps, captured as CUDA graphs of back
+to back calls and timed with CUDA events on the capture stream.  Consecutive
+calls rotate over enough copies of the packed weights that the working set is
+more than 4x the L2 (each copy is re-read only after >500 MB of other reads).
+SM clocks and throttle reasons are sampled with nvidia-smi during the run.
+
+Also reported in the same JSON line: the GEMV kernel alone against the HBM
+roofline, batch 4, the end-to-end figure through the public API with host
+buffers (activations H2D and outputs D2H inside the timed region), and the
+CPU oracle timed on a bounded sample on the host cores (cpu_baseline).
+
+``--impl reference`` times the CPU oracle alone (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+M_DEC, K_DEC = 14336, 4096
+WEIGHT_BYTES = M_DEC * K_DEC // 32 * 10
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "ROCmFP2 GEMV packed-weight GB/s (% HBM peak); prefill GEMM TOPS (% peak)"
+WORKLOAD = ("rocmfp2 decode GEMV 14336x4096, batch 1, fp32 activations quantized in the call "
+            "(Student-t(5)*0.02 weights, 41 outlier columns x8, seed 1)")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "measured (MEASURED_PEAKS.json)"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback (no MEASURED_PEAKS.json)"}
+
+
+# ---------------------------------------------------------------------------
+# clocks
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if ts < t0 - 0.2 or ts > t1 + 0.2:
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+
+
+def _graph_time_ms(torch, fn, calls: int, reps: int = 1):
+    """Capture `calls` invocations of fn(i) in one CUDA graph; return the
+    per-call time (ms) of `reps` replays timed with events on the stream."""
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn(0)  # prime outside capture (library init, smem attributes)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(calls):
+                fn(i)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / (calls * reps), g, stream
+
+
+def run_gpu(args):
+    import torch
+    import gemm_rocmfp2_mul_gb300 as gl
+    from synth import decode_gemv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    gl.build()
+    gl.lib()
+    peaks = load_peaks()
+
+    # ---- data (untimed): synthetic weights packed on the GPU, copies for L2 rotation
+    w = decode_gemv(N=4)
+    Wd = torch.from_numpy(w["W"]).cuda()
+    P = gl.rfp2_pack_weights(Wd)
+    del Wd
+    copies = max(4, -(-4 * L2_BYTES // WEIGHT_BYTES))
+    copies = 1 << (copies - 1).bit_length()
+    Pc = torch.empty((copies,) + tuple(P.shape), dtype=torch.uint8, device="cuda")
+    Pc[:] = P
+    x1 = torch.from_numpy(w["x"][:1]).cuda()
+    x4 = torch.from_numpy(w["x"][:4]).cuda()
+    y1 = torch.empty((1, M_DEC), dtype=torch.float32, device="cuda")
+    y4 = torch.empty((4, M_DEC), dtype=torch.float32, device="cuda")
+    ws1 = torch.empty(gl.rfp2_gemv_workspace_bytes(1, K_DEC), dtype=torch.uint8, device="cuda")
+    ws4 = torch.empty(gl.rfp2_gemv_workspace_bytes(4, K_DEC), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step1(i):
+        gl.rfp2_gemv(Pc[i % copies], M_DEC, K_DEC, x1, y=y1, workspace=ws1, dev_status=st)
+
+    def step4(i):
+        gl.rfp2_gemv(Pc[i % copies], M_DEC, K_DEC, x4, y=y4, workspace=ws4, dev_status=st)
+
+    q1, d1 = gl.rfp2_quantize_act(x1)
+
+    def kern1(i):
+        gl.rfp2_gemv_q8(Pc[i % copies], M_DEC, K_DEC, q1, d1, y=y1, dev_status=st)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+
+    # ---- warm-up: W steps (plus a short clock ramp of the same calls)
+    G = min(args.steps, 1000)
+    _, gw, sw = _graph_time_ms(torch, step1, max(args.warmup, 3))
+    t_ramp = time.time()
+    while time.time() - t_ramp < 1.0:
+        gw.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed: exactly K steps (graphs of G calls + one remainder graph)
+    full, rem = divmod(args.steps, G)
+    ms_g, gg, sg = _graph_time_ms(torch, step1, G)
+    graphs = [(gg, sg)] * full
+    if rem:
+        _, gr, sr = _graph_time_ms(torch, step1, rem)
+        graphs.append((gr, sr))
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    main_stream = sg
+    with torch.cuda.stream(main_stream):
+        start.record(main_stream)
+        for g_, s_ in graphs:
+            g_.replay()
+        end.record(main_stream)
+    end.synchronize()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    total_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * WEIGHT_BYTES / (ms_per_step * 1e-3) / 1e9
+
+    # ---- the GEMV kernel alone (roofline) and batch 4
+    kreps = max(1, 5000 // G)
+    ms_k, _, _ = _graph_time_ms(torch, kern1, G, reps=kreps)
+    ms_b4, _, _ = _graph_time_ms(torch, step4, G, reps=kreps)
+    clocks.stop()
+    clk = clocks.summary(t_ramp, time.time())
+    status = int(st.item())
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(torch, gl, w, Pc, copies, args.steps)
+
+    achieved = WEIGHT_BYTES / (ms_k * 1e-3) / 1e9
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "i8",
+        "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD,
+            "M": M_DEC, "K": K_DEC, "batch": 1,
+            "bytes_per_step": WEIGHT_BYTES,
+            "l2": f"inputs larger than L2: {copies} rotating weight copies "
+                  f"({copies * WEIGHT_BYTES / 1e6:.0f} MB > 129 MB L2)",
+            "timing": f"CUDA graphs of {G} back-to-back calls, CUDA events on the capture stream",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "gemv_q8_kernel<1,4> (weights streamed by bulk async copies)",
+            "achieved": round(achieved, 1),
+            "peak": peaks["hbm_gbs"],
+            "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": args.traffic,
+            "peak_source": peaks["source"] + " hbm_gbs",
+            "us_per_launch": round(ms_k * 1e3, 3),
+        },
+        "secondary": {
+            "decode_batch4": {
+                "GB_per_s": round(WEIGHT_BYTES / (ms_b4 * 1e-3) / 1e9, 1),
+                "us_per_call": round(ms_b4 * 1e3, 3),
+                "frac_of_hbm_peak": round(WEIGHT_BYTES / (ms_b4 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            },
+            "call_us_batch1": round(ms_per_step * 1e3, 3),
+        },
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "dev_status": status,
+    }
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(torch, gl, w, Pc, copies, steps):
+    """Same metric through the public API with the activations in pinned host
+    memory: each step copies x H2D, runs rfp2_gemv and copies y D2H."""
+    x_h = torch.from_numpy(w["x"][:1].copy()).pin_memory()
+    y_h = torch.empty((1, M_DEC), dtype=torch.float32).pin_memory()
+    x_d = torch.empty((1, K_DEC), dtype=torch.float32, device="cuda")
+    y_d = torch.empty((1, M_DEC), dtype=torch.float32, device="cuda")
+    ws = torch.empty(gl.rfp2_gemv_workspace_bytes(1, K_DEC), dtype=torch.uint8, device="cuda")
+
+    def step(i):
+        x_d.copy_(x_h, non_blocking=True)
+        gl.rfp2_gemv(Pc[i % copies], M_DEC, K_DEC, x_d, y=y_d, workspace=ws)
+        y_h.copy_(y_d, non_blocking=True)
+
+    G = min(steps, 1000)
+    ms, g, s = _graph_time_ms(torch, step, G, reps=max(1, steps // G))
+    return {"value": round(WEIGHT_BYTES / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": 1 * K_DEC * 4, "d2h_bytes_per_step": 1 * M_DEC * 4,
+            "us_per_step": round(ms * 1e3, 3)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+
+
+def _oracle_sample(rows: int):
+    import oracle
+    from synth import decode_gemv
+    w = decode_gemv(N=1)
+    idx = np.linspace(0, M_DEC - 1, rows).astype(np.int64)
+    P = oracle.rfp2_pack(w["W"][idx])
+    return oracle, P, w["x"][:1].copy(), idx
+
+
+def cpu_baseline(seconds: float, rows: int = 512):
+    """The oracle (single-threaded C, fp64 dots) timed on a bounded sample of
+    the same workload: quantize x + GEMV over `rows` sampled weight rows,
+    repeated for about `seconds`; scaled to packed-weight GB/s."""
+    orc, P, x, idx = _oracle_sample(rows)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        q, d = orc.quantize_act(x)
+        orc.rfp2_gemv(P, rows, K_DEC, q, d)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    bytes_done = n * rows * K_DEC // 32 * 10
+    return {"value": round(bytes_done / dt / 1e9, 6), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{n} x (quantize x + GEMV over {rows} of {M_DEC} rows), {dt:.1f} s"}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle on the host cores, exactly K steps after W
+    warm-up steps; each step is quantize + GEMV over a row sample sized so the
+    whole run stays within about a minute."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    orc, P, x, idx = _oracle_sample(64)
+    t0 = time.perf_counter()
+    q, d = orc.quantize_act(x)
+    orc.rfp2_gemv(P, 64, K_DEC, q, d)
+    per_row = (time.perf_counter() - t0) / 64
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    rows = int(min(M_DEC, max(8, budget / max(per_row, 1e-9))))
+    orc, P, x, idx = _oracle_sample(rows)
+    for _ in range(args.warmup):
+        q, d = orc.quantize_act(x)
+        orc.rfp2_gemv(P, rows, K_DEC, q, d)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        q, d = orc.quantize_act(x)
+        orc.rfp2_gemv(P, rows, K_DEC, q, d)
+    dt = time.perf_counter() - t0
+    value = args.steps * rows * K_DEC // 32 * 10 / dt / 1e9
+    sample = f"each step = quantize x + GEMV over {rows} of {M_DEC} rows ({dt:.1f} s total)"
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M_DEC, "K": K_DEC, "batch": 1,
+                   "reference": "CPU oracle (plain C, fp64), bounded row sample"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per GEMV launch from an ncu capture of this kernel")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,317 @@
+// Dense ROCmFP2 GEMV: y[n, m] = sum_k w[m, k] * q[n, k] * dA (int8 path).
+//
+// Source: "ROCmFP2 codebook research report", sections "01 Storage",
+// "02 Quantization" and "03 Runtime" (LOAD -> SPREAD -> PERMUTE -> DOT4 ->
+// RESCALE, with each block expanded once for every activation column).
+//
+// GB300 design.  The packed weights (2.5 bits per weight) are the only large
+// stream, so the kernel is built around HBM:
+//  * Persistent grid, one CTA per SM; CTA i owns the contiguous rows
+//    [i*M/G, (i+1)*M/G), so its weights are one contiguous slab.
+//  * A producer warp streams that slab into a ring of shared-memory stages
+//    with 1-D bulk async copies (cp.async.bulk, L2 evict-first), one stage per
+//    chunk of rows, issuing as many stages as fit (~200 KB) before the first
+//    one is consumed.  Rows of K % 256 == 0 are whole 16-byte units.
+//  * Twelve consumer warps.  Each thread keeps the int8 activations of its
+//    K-slice for all N columns in registers, reads its BPT blocks of a row
+//    with conflict-free shared loads (strides 20/40/80 B map to distinct
+//    banks) and runs the PRMT + dp4a decode of rfp2_decode.cuh.
+//  * Every wait is an mbarrier wait with a time limit; a timeout stores
+//    RFP2_ETIMEOUT and the CTA winds down after its copies have landed.  The
+//    cross-warp reduction (when a row spans several warps) also goes through
+//    mbarriers, never through bar.sync, so no wait can hang.
+#include <mutex>
+
+#include "common.cuh"
+#include "gemv_core.cuh"
+#include "quantize.cuh"
+
+namespace rfp2 {
+namespace {
+
+// Consumer warps per CTA (+ 1 producer warp).  Batch 1 needs about 70
+// registers per thread, so 16 consumer warps fit (the 544-thread block is
+// capped at 96 registers); wider batches hold more activations and use 12
+// (416 threads, 128 registers).
+#ifndef RFP2_GEMV_WARPS1
+#define RFP2_GEMV_WARPS1 16
+#endif
+#ifndef RFP2_GEMV_WARPS
+#define RFP2_GEMV_WARPS 12
+#endif
+#ifndef RFP2_GEMV_MAX_STAGES
+#define RFP2_GEMV_MAX_STAGES 64
+#endif
+template <int NC>
+constexpr int consumer_warps() {
+    return NC == 1 ? RFP2_GEMV_WARPS1 : RFP2_GEMV_WARPS;
+}
+template <int NC>
+constexpr int gemv_threads() {
+    return (consumer_warps<NC>() + 1) * 32;
+}
+
+// Rows per warp per chunk: several independent rows per warp amortise the
+// per-chunk wait, reduction and bookkeeping; capped so R*NC <= 8.
+#ifndef RFP2_GEMV_R1
+#define RFP2_GEMV_R1 2
+#endif
+template <int NC>
+constexpr int rows_per_warp() {
+    return NC == 1 ? RFP2_GEMV_R1 : NC == 2 ? 2 : 1;
+}
+
+template <int NC, int BPT>
+__global__ void __launch_bounds__(gemv_threads<NC>(), 1)
+    gemv_q8_kernel(const uint8_t *__restrict__ W, int M, int K, const int8_t *__restrict__ q,
+                   const float *__restrict__ d, float *__restrict__ y, int32_t *status, int WK,
+                   int stages, int rows_per_cta, int rows_extra) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int KB = K >> 5;
+    const int rowbytes = KB * 10;
+    constexpr int R = rows_per_warp<NC>();
+    constexpr int CW = consumer_warps<NC>();
+    const int RG = CW / WK;  // row groups; R rows per group per chunk
+    const int CR = RG * R;   // rows per chunk
+    Ring r = carve_ring(smem, stages, CR * rowbytes, RG, WK, NextPow2<R * NC>::v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // CTA i owns rows_per_cta (+1 for the first rows_extra CTAs) contiguous rows
+    const int bx = blockIdx.x;
+    const int64_t r_begin = (int64_t)bx * rows_per_cta + min(bx, rows_extra);
+    const int nrows = rows_per_cta + (bx < rows_extra ? 1 : 0);
+    const int64_t r_end = r_begin + nrows;
+    const int nchunks = (nrows + CR - 1) / CR;
+    const uint8_t *src = W + r_begin * rowbytes;
+    const bool producer = warp == CW && lane == 0;
+    uint64_t pol = 0;
+    int c = 0;
+    // activations staged after the ring: q [NC, K] int8 then d [NC, K/32] fp32
+    const uint32_t qbytes = (uint32_t)NC * K, dbytes = (uint32_t)NC * KB * 4;
+    uint8_t *act_q = smem + ring_bytes(stages, CR * rowbytes, RG, WK, NextPow2<R * NC>::v);
+    uint8_t *act_d = act_q + ((qbytes + 15) & ~15u);
+    if (producer) {
+        // start the weight stream before anything else: the stage barriers
+        // are initialised and the first stages issued ahead of the CTA barrier
+        init_ring_stages(r, CW);
+        pol = policy_evict_first();
+        for (; c < nchunks && c < stages; ++c) {
+            const int rows = min(CR, nrows - c * CR);
+            produce_chunk(r, c, src + (int64_t)c * CR * rowbytes, (uint32_t)(rows * rowbytes), pol,
+                          status);
+        }
+    }
+    init_ring_reduction(r, threadIdx.x, CW * 32);
+    __syncthreads();
+
+    if (warp == CW) {
+        // q and d may come from the kernel launched just before this one
+        pdl_wait();
+        load_act_to_smem(r, lane, act_q, q, qbytes, act_d, d, dbytes);
+        // producer: refill the ring as the consumers release stages
+        if (lane == 0) {
+            for (; c < nchunks; ++c) {
+                const int rows = min(CR, nrows - c * CR);
+                if (!produce_chunk(r, c, src + (int64_t)c * CR * rowbytes,
+                                   (uint32_t)(rows * rowbytes), pol, status))
+                    break;
+            }
+            drain_ring(r, c, status);
+        }
+        return;
+    }
+
+    const int wg = warp / WK, wk = warp % WK;
+    const int kb0 = (wk * 32 + lane) * BPT;
+    const bool active = kb0 < KB;
+    pdl_wait();
+    pdl_launch_dependents();
+    if (!mbar_wait(r.act_bar, 0)) {
+        record_status(status, RFP2_ETIMEOUT);
+        *r.abort_flag = 1;
+        return;
+    }
+    Act<NC, BPT> A;
+    int cols[NC];
+    float *ycol[NC];
+#pragma unroll
+    for (int n = 0; n < NC; ++n) {
+        cols[n] = n;
+        ycol[n] = y + (int64_t)n * M;
+    }
+    load_act<NC, BPT, true>(A, reinterpret_cast<const int8_t *>(act_q),
+                      reinterpret_cast<const float *>(act_d), K, kb0, active, cols);
+    for (c = 0; c < nchunks; ++c) {
+        int64_t rows[R];
+        bool valid[R];
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            rows[rr] = r_begin + (int64_t)c * CR + wg * R + rr;
+            valid[rr] = rows[rr] < r_end;
+        }
+        if (!consume_chunk<NC, BPT, R>(r, c, wg, wk, lane, kb0, active, rowbytes, rows, valid, A,
+                                       ycol, status))
+            break;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+
+struct Plan {
+    int bpt, WK, RG, chunk_bytes, stages, grid;
+    size_t smem;
+};
+
+bool make_plan(int NC, int64_t M, int64_t K, Plan &p) {
+    const int KB = (int)(K / 32);
+    int bpt = bpt_max(NC);
+    while (bpt > 1 && KB < 32 * bpt) bpt /= 2;
+    int WK = (KB + 32 * bpt - 1) / (32 * bpt);
+    // K-slice warps per row: the smallest divisor of the consumer warp count
+    // that covers the row (row groups of CW / WK warps)
+    const int CW = NC == 1 ? consumer_warps<1>() : consumer_warps<2>();
+    int WKp = 0;
+    for (int dv = 1; dv <= CW; ++dv)
+        if (CW % dv == 0 && dv >= WK) {
+            WKp = dv;
+            break;
+        }
+    if (WKp == 0) return false;
+    p.bpt = bpt;
+    p.WK = WKp;
+    p.RG = CW / WKp;
+    const int R = NC == 1 ? rows_per_warp<1>() : NC == 2 ? rows_per_warp<2>() : 1;
+    const int CR = p.RG * R;
+    const int rowbytes = KB * 10;
+    p.chunk_bytes = CR * rowbytes;
+    const int64_t chunks_total = (M + CR - 1) / CR;
+    const int sms = sm_count(current_device());
+    p.grid = (int)(chunks_total < sms ? chunks_total : sms);
+    const int64_t rows_per_cta = (M + p.grid - 1) / p.grid;
+    const int chunks_per_cta = (int)((rows_per_cta + CR - 1) / CR);
+    const int RN = R * NC;
+    const int V = RN <= 1 ? 1 : RN <= 2 ? 2 : RN <= 4 ? 4 : 8;
+    const size_t act = ((size_t)NC * K + 15) / 16 * 16 + (size_t)NC * KB * 4;
+    int stages = chunks_per_cta < RFP2_GEMV_MAX_STAGES ? chunks_per_cta : RFP2_GEMV_MAX_STAGES;
+    while (stages > 1 &&
+           ring_bytes(stages, p.chunk_bytes, p.RG, p.WK, V) + act > (size_t)kGemvSmemBudget)
+        --stages;
+    p.stages = stages;
+    p.smem = ring_bytes(stages, p.chunk_bytes, p.RG, p.WK, V) + act;
+    return p.smem <= 227 * 1024;
+}
+
+template <int NC, int BPT>
+cudaError_t launch_gemv_t(const Plan &p, const uint8_t *W, int M, int K, const int8_t *q,
+                          const float *d, float *y, int32_t *status, cudaStream_t stream,
+                          bool pdl) {
+    auto kern = gemv_q8_kernel<NC, BPT>;
+    static std::mutex mu;
+    static int configured[64] = {0};
+    const int dev = current_device();
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && configured[dev] == 0) {
+            cudaError_t e = set_smem_limit(kern, 227 * 1024);
+            if (e != cudaSuccess) return e;
+            configured[dev] = 1;
+        }
+    }
+    return launch(kern, dim3(p.grid), dim3(gemv_threads<NC>()), p.smem, stream, pdl, W, M, K, q, d, y,
+                  status, p.WK, p.stages, M / p.grid, M % p.grid);
+}
+
+template <int NC>
+cudaError_t launch_gemv_nc(const Plan &p, const uint8_t *W, int M, int K, const int8_t *q,
+                           const float *d, float *y, int32_t *status, cudaStream_t stream,
+                           bool pdl) {
+    switch (p.bpt) {
+        case 8:
+            if constexpr (bpt_max(NC) >= 8)
+                return launch_gemv_t<NC, 8>(p, W, M, K, q, d, y, status, stream, pdl);
+            break;
+        case 4:
+            if constexpr (bpt_max(NC) >= 4)
+                return launch_gemv_t<NC, 4>(p, W, M, K, q, d, y, status, stream, pdl);
+            break;
+        case 2:
+            if constexpr (bpt_max(NC) >= 2)
+                return launch_gemv_t<NC, 2>(p, W, M, K, q, d, y, status, stream, pdl);
+            break;
+        default:
+            return launch_gemv_t<NC, 1>(p, W, M, K, q, d, y, status, stream, pdl);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemv(const uint8_t *W, int64_t M, int64_t K, const int8_t *q, const float *d,
+                        int64_t N, float *y, int32_t *status, cudaStream_t stream, bool pdl) {
+    Plan p;
+    if (!make_plan((int)N, M, K, p)) return cudaErrorInvalidValue;
+    const int m = (int)M, k = (int)K;
+    switch (N) {
+        case 1: return launch_gemv_nc<1>(p, W, m, k, q, d, y, status, stream, pdl);
+        case 2: return launch_gemv_nc<2>(p, W, m, k, q, d, y, status, stream, pdl);
+        case 3: return launch_gemv_nc<3>(p, W, m, k, q, d, y, status, stream, pdl);
+        case 4: return launch_gemv_nc<4>(p, W, m, k, q, d, y, status, stream, pdl);
+        case 5: return launch_gemv_nc<5>(p, W, m, k, q, d, y, status, stream, pdl);
+        case 6: return launch_gemv_nc<6>(p, W, m, k, q, d, y, status, stream, pdl);
+        case 7: return launch_gemv_nc<7>(p, W, m, k, q, d, y, status, stream, pdl);
+        case 8: return launch_gemv_nc<8>(p, W, m, k, q, d, y, status, stream, pdl);
+    }
+    return cudaErrorInvalidValue;
+}
+
+rfp2_status check_gemv_shape(int64_t M, int64_t K, int64_t N) {
+    if (M <= 0 || K <= 0 || N < 1 || N > RFP2_MAX_BATCH) return RFP2_ESHAPE;
+    if (M > (1LL << 30) || K > (1LL << 30)) return RFP2_ESHAPE;
+    if (K % 256 != 0) return RFP2_EUNSUPPORTED;
+    Plan p;
+    if (!make_plan((int)N, M, K, p)) return RFP2_EUNSUPPORTED;
+    return RFP2_OK;
+}
+
+}  // namespace
+
+size_t gemv_workspace_bytes(int64_t N, int64_t K) {
+    const size_t qb = ((size_t)(N * K) + 255) / 256 * 256;
+    return qb + (size_t)(N * (K / 32)) * sizeof(float);
+}
+
+}  // namespace rfp2
+
+using namespace rfp2;
+
+extern "C" rfp2_status rfp2_gemv_q8(const uint8_t *W, int64_t M, int64_t K, const int8_t *q,
+                                    const float *d, int64_t N, float *y, int32_t *dev_status,
+                                    rfp2_stream_t stream) {
+    if (!W || !q || !d || !y) return RFP2_EINVAL;
+    const rfp2_status st = check_gemv_shape(M, K, N);
+    if (st != RFP2_OK) return st;
+    if (!aligned(W, 16) || !aligned(q, 16) || !aligned(d, 16) || !aligned(y, 4)) return RFP2_EALIGN;
+    return from_cuda(launch_gemv(W, M, K, q, d, N, y, dev_status,
+                                 reinterpret_cast<cudaStream_t>(stream), false));
+}
+
+extern "C" size_t rfp2_gemv_workspace_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0) return 0;
+    return gemv_workspace_bytes(N, K);
+}
+
+extern "C" rfp2_status rfp2_gemv(const uint8_t *W, int64_t M, int64_t K, const float *x,
+                                 int64_t N, float *y, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, rfp2_stream_t stream) {
+    if (!W || !x || !y) return RFP2_EINVAL;
+    const rfp2_status st = check_gemv_shape(M, K, N);
+    if (st != RFP2_OK) return st;
+    if (!workspace || workspace_bytes < gemv_workspace_bytes(N, K)) return RFP2_EWORKSPACE;
+    if (!aligned(W, 16) || !aligned(x, 4) || !aligned(y, 4) || !aligned(workspace, 256))
+        return RFP2_EALIGN;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int8_t *q = static_cast<int8_t *>(workspace);
+    float *d = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                         ((size_t)(N * K) + 255) / 256 * 256);
+    cudaError_t e = launch_quantize(x, N, K, q, d, s, true);
+    if (e != cudaSuccess) return RFP2_ECUDA;
+    return from_cuda(launch_gemv(W, M, K, q, d, N, y, dev_status, s, true));
+}

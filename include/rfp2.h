@@ -1,0 +1,209 @@
+/*
+ * rfp2.h - C ABI of librfp2.so: block-quantized (ROCmFP2, HFP4G32) GEMV and
+ * GEMM on one NVIDIA GB300 (sm_103a).
+ *
+ * Formats (sources named by page title and section):
+ *  - ROCmFP2 block: "ROCmFP2 codebook research report", section "01 Storage".
+ *    Ten bytes per 32 weights: q0..q7 hold four 2-bit selectors each,
+ *    little-endian (weight 4j+i in bits 2i..2i+1 of byte j), then e0 (scale of
+ *    weights 0-15) and e1 (weights 16-31).  A matrix W [M, K] is stored as
+ *    uint8 [M, K/32, 10]: blocks row-major, rows contiguous, no row header.
+ *  - Codebook (section "02 Quantization"): code 00 -> -4, 01 -> -1,
+ *    10 -> +1, 11 -> +4.  Weight = codebook[code] * scale.
+ *  - UE4M3 scale byte (section "02 Quantization"): E = b >> 3, M = b & 7;
+ *    E = 0 -> M * 2^-10, else (8 + M) * 2^(E - 11).  Bytes 0x00..0x7E are
+ *    legal; 0x7F and above are invalid.
+ *  - Q8_1-style activations (section "03 Runtime" names Q8_1 activations):
+ *    per 32 values d = max|a| / 127 (fp32), q = round-half-away(a / d)
+ *    clamped to +-127, q = 0 when d == 0.  q int8 [N, K], d fp32 [N, K/32].
+ *  - HFP4G32 row: "HFP4" (hipfire.dev), section "Byte layout - HFP4G32":
+ *    16-byte header (f16 row_scale_a, f16 row_scale_b = 0, u16 K/32, u8
+ *    flags, reserved) then K/32 blocks of (UE8M0 byte, 16 bytes of E2M1
+ *    nibbles, element 2b in the low nibble of byte b).  Row bytes
+ *    16 + 17*K/32.  Value = row_scale_a * 2^(e - 127) * E2M1[nibble]
+ *    (section "Per-row second-level scale (FP16)"); block byte 0xFF is NaN.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are device memory owned by the caller unless the comment says
+ *    host.  The library never allocates device memory and never frees the
+ *    caller's buffers.  Arrays are row-major and contiguous.
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream) and
+ *    return after enqueueing.  The return value reports host-side argument
+ *    checks and launch errors only; outputs are valid after the stream
+ *    reaches the enqueued work.
+ *  - `dev_status` (optional, may be NULL) is one int32 in device memory.  A
+ *    kernel that detects an error on the device (a routing id out of range, a
+ *    bounded wait that ran out) stores the matching rfp2_status code there;
+ *    it never clears it.  The caller zeroes it before the call and reads it
+ *    after synchronizing.  With NULL, device-detected errors go unreported.
+ *  - Inputs and outputs must not overlap.  Weights are assumed to hold only
+ *    legal scale bytes (check with rfp2_validate_weights); an illegal byte
+ *    gives unspecified values in the affected outputs, never a fault.
+ *  - GPU kernels need K % 256 == 0 (so a row of packed weights is a whole
+ *    number of 16-byte units); other K return RFP2_EUNSUPPORTED.
+ */
+#ifndef RFP2_H
+#define RFP2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque stream handle: pass a cudaStream_t. */
+typedef struct CUstream_st *rfp2_stream_t;
+
+typedef enum {
+    RFP2_OK = 0,
+    RFP2_EINVAL = 1,        /* null pointer, negative size, bad enum */
+    RFP2_ESHAPE = 2,        /* inconsistent or out-of-range sizes */
+    RFP2_EALIGN = 3,        /* a pointer is not aligned as documented */
+    RFP2_EUNSUPPORTED = 4,  /* valid input outside what the kernels support */
+    RFP2_ECUDA = 5,         /* a CUDA runtime call failed */
+    RFP2_EBADSCALE = 6,     /* an illegal scale byte was found */
+    RFP2_EBADID = 7,        /* a routing id outside [0, E) */
+    RFP2_ETIMEOUT = 8,      /* a bounded device wait ran out */
+    RFP2_EWORKSPACE = 9     /* workspace missing or too small */
+} rfp2_status;
+
+/* Static string naming a status code ("RFP2_OK", ...). */
+const char *rfp2_status_str(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int rfp2_version(void);
+
+/* Largest batch (activation columns) the GEMV entry points take. */
+#define RFP2_MAX_BATCH 8
+
+/* ---------------------------------------------------------------------------
+ * Activation quantization (Q8_1-style blocks, "03 Runtime").
+ *   x  fp32 [N, K] device, K % 32 == 0 (K % 256 == 0 not required here).
+ *   q  int8 [N, K] device (output).  d fp32 [N, K/32] device (output).
+ * Errors: EINVAL (null, N or K < 0), ESHAPE (K % 32), ECUDA.
+ */
+rfp2_status rfp2_quantize_act(const float *x, int64_t N, int64_t K, int8_t *q, float *d,
+                              rfp2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * ROCmFP2 GEMV on already-quantized activations ("03 Runtime": expand each
+ * code byte to four signed int8 lanes, integer dot against Q8_1 activations,
+ * int32 sum per 16-weight half, then y += dA * (d0 * S0 + d1 * S1)).
+ *   W  uint8 [M, K/32, 10] device, 16-byte aligned.
+ *   q  int8 [N, K], d fp32 [N, K/32] device (from rfp2_quantize_act), both
+ *      16-byte aligned.
+ *   y  fp32 [N, M] device (output), y[n, m] = sum over row m of W times
+ *      column n.  1 <= N <= RFP2_MAX_BATCH.  Each weight block is expanded
+ *      once and reused for all N columns ("03 Runtime", multi-column reuse).
+ * Errors: EINVAL, ESHAPE (N out of range, M or K <= 0), EUNSUPPORTED
+ * (K % 256), EALIGN (W, q or d not 16-byte aligned), ECUDA.
+ */
+rfp2_status rfp2_gemv_q8(const uint8_t *W, int64_t M, int64_t K, const int8_t *q,
+                         const float *d, int64_t N, float *y, int32_t *dev_status,
+                         rfp2_stream_t stream);
+
+/* Bytes of workspace rfp2_gemv needs for N columns of length K. */
+size_t rfp2_gemv_workspace_bytes(int64_t N, int64_t K);
+
+/* ---------------------------------------------------------------------------
+ * ROCmFP2 GEMV from fp32 activations: quantizes x into `workspace` (q then
+ * d) and runs the GEMV, as two launches chained with programmatic dependent
+ * launch so the weight stream starts while x is quantized.
+ *   x fp32 [N, K] device; y fp32 [N, M] device; workspace device, at least
+ *   rfp2_gemv_workspace_bytes(N, K) bytes, 256-byte aligned; after the call
+ *   it holds q int8 [N, K] followed (at offset rounded up to 256) by d.
+ * Errors: as rfp2_gemv_q8, plus EWORKSPACE.
+ */
+rfp2_status rfp2_gemv(const uint8_t *W, int64_t M, int64_t K, const float *x, int64_t N,
+                      float *y, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                      rfp2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * MoE bulk-expert GEMV (MUL_MAT_ID over the routed experts' rows for a few
+ * tokens: "HRX on the Radeon iGPU", section "MoE decode and the kernel
+ * cache").
+ *   W    uint8 [E, M, K/32, 10] device (E experts, each an M x K ROCmFP2
+ *        matrix), 16-byte aligned.
+ *   ids  int32 [T, top_k] device: the experts of each token.
+ *   x    fp32 [T, K] device.
+ *   y    fp32 [T, top_k, M] device (output): y[t, j, :] = W[ids[t, j]] x_t.
+ *   Each token is quantized once; each touched expert's blocks are expanded
+ *   once for all of its tokens.  1 <= T*top_k <= 4096, E <= 65536.
+ *   workspace: rfp2_moe_workspace_bytes(T, top_k, K) bytes, 256-byte aligned.
+ * An id outside [0, E) is never dereferenced: its output row y[t, j, :] is
+ * filled with NaN and RFP2_EBADID is stored to *dev_status.
+ * Errors: EINVAL, ESHAPE, EUNSUPPORTED (K % 256), EALIGN, EWORKSPACE, ECUDA.
+ */
+size_t rfp2_moe_workspace_bytes(int64_t T, int64_t top_k, int64_t K);
+rfp2_status rfp2_moe_gemv(const uint8_t *W, int64_t E, int64_t M, int64_t K,
+                          const int32_t *ids, int64_t T, int64_t top_k, const float *x,
+                          float *y, void *workspace, size_t workspace_bytes,
+                          int32_t *dev_status, rfp2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Prefill GEMM on the tensor cores ("ROCmFP2 codebook research report",
+ * section "04 Measured evidence": the end-to-end gain comes from prefill).
+ * Y[n, m] = sum_k X[n, k] * w[m, k], with w = codebook * scale expanded
+ * exactly to bf16 (at most 4 significant bits times a power of two) and fp32
+ * accumulation in tensor memory.  No activation quantization on this path.
+ *   W  uint8 [M, K/32, 10] device.  X bf16 bits [N, K] device, 16-byte
+ *   aligned.  Y fp32 [N, M] device (output), 16-byte aligned.
+ *   M % 16 == 0, N >= 1, K % 256 == 0.
+ *   workspace: rfp2_gemm_workspace_bytes(M, K) bytes, 1024-byte aligned
+ *   (holds the expanded bf16 weights [M, K]).
+ * Errors: EINVAL, ESHAPE, EUNSUPPORTED, EALIGN, EWORKSPACE, ECUDA.
+ */
+size_t rfp2_gemm_workspace_bytes(int64_t M, int64_t K);
+rfp2_status rfp2_gemm(const uint8_t *W, int64_t M, int64_t K, const uint16_t *X, int64_t N,
+                      float *Y, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                      rfp2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * HFP4G32 GEMV ("HFP4", sections "Per-row second-level scale (FP16)" and
+ * "v1 correctness-anchor inner loop"): y[n, m] = row_scale_a(m) *
+ * sum_b 2^(e_b - 127) * sum_i E2M1[c_i] * x[n, i], fp32 activations, fp32
+ * accumulation, row scale applied once at the end of the row.
+ *   W  uint8 [M, 16 + 17*K/32] device, 16-byte aligned; x fp32 [N, K];
+ *   y fp32 [N, M] (output).  1 <= N <= RFP2_MAX_BATCH, K % 256 == 0.
+ * Errors: EINVAL, ESHAPE, EUNSUPPORTED, EALIGN, ECUDA.
+ */
+rfp2_status hfp4_gemv(const uint8_t *W, int64_t M, int64_t K, const float *x, int64_t N,
+                      float *y, int32_t *dev_status, rfp2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Weight packers (offline preparation; "02 Quantization" for ROCmFP2 and
+ * "Quantization recipe (HFP4G32)" for HFP4).  Output is bit-identical to the
+ * CPU oracle's packers.
+ *  rfp2_pack_weights: W fp32 [M, K] (finite, K % 32 == 0) -> out uint8
+ *    [M, K/32, 10].  Each 16-weight half tries every legal UE4M3 byte in
+ *    ascending order, picks codes by sign and fp32 |x/s| <= 2.5, and keeps
+ *    the first byte with the lowest fp64 squared error.  Non-finite inputs
+ *    are a contract violation (their blocks get unspecified bytes).
+ *  hfp4_pack_weights: W fp32 [M, K] -> out uint8 [M, 16 + 17*K/32]:
+ *    row_scale_a = fp16(max|W|/6), smallest block exponent with
+ *    block max <= 6 * 2^(e-127), nearest E2M1 code (ties to even mantissa).
+ *    Rows whose max|W|/6 overflows fp16 store RFP2_EINVAL to *dev_status.
+ * Errors: EINVAL, ESHAPE, ECUDA.
+ */
+rfp2_status rfp2_pack_weights(const float *W, int64_t M, int64_t K, uint8_t *out,
+                              rfp2_stream_t stream);
+rfp2_status hfp4_pack_weights(const float *W, int64_t M, int64_t K, uint8_t *out,
+                              int32_t *dev_status, rfp2_stream_t stream);
+
+/* Counts scale bytes >= 0x7F in nblocks packed ROCmFP2 blocks: adds the count
+ * to *bad_count (device int64, caller zeroes it) and stores RFP2_EBADSCALE
+ * to *dev_status (optional) if any was found. */
+rfp2_status rfp2_validate_weights(const uint8_t *W, int64_t nblocks, int64_t *bad_count,
+                                  int32_t *dev_status, rfp2_stream_t stream);
+
+/* Debug / test: every int32 half sum of the GEMV's integer path,
+ * partials[n, m, h] = sum_{i<16} codebook[code(m, 16h+i)] * q[n, 16h+i],
+ * int32 [N, M, K/16] device.  Uses the same expansion code as the GEMV. */
+rfp2_status rfp2_debug_half_partials(const uint8_t *W, int64_t M, int64_t K, const int8_t *q,
+                                     int64_t N, int32_t *partials, rfp2_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RFP2_H */

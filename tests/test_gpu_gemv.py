@@ -1,0 +1,284 @@
+"""GPU parity of the activation quantizer, the packers, the int32 half sums and
+the dense ROCmFP2 GEMV against the CPU oracle, through the C ABI.
+
+Bar (statement of the problem): packed bytes, int8 activations, their scales
+and every int32 half sum bit-exact; fp32 outputs within 1e-5 relative,
+normwise per output row (one token's [M] vector), of the fp64 oracle.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from synth import child_rngs, decode_gemv, hfp4_gemv, normal_weights, tiny_gemv
+from _helpers import rel_err_rows
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def g():
+    import gemm_rocmfp2_mul_gb300 as g
+    g.build()
+    g.lib()
+    return g
+
+
+def dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    import torch
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def status_tensor():
+    import torch
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def _inputs(kind, N, K, seed=0):
+    rng = np.random.default_rng(seed)
+    if kind == "normal":
+        x = rng.normal(0, 1, (N, K))
+    elif kind == "student_t":
+        x = rng.standard_t(3, (N, K)) * 1e-3
+    elif kind == "wide":
+        x = rng.normal(0, 1, (N, K)) * 10.0 ** rng.integers(-6, 6, (N, K // 32, 1)).repeat(32, 2).reshape(N, K)
+    else:
+        x = rng.normal(0, 1, (N, K))
+        x[:, :64] = 0.0
+        x[:, 64:96] = -0.0
+        # exact halves: block max 127 -> d = 1, values k + 0.5 tie away from zero
+        x[:, 96:128] = np.arange(-16, 16) + 0.5
+        x[:, 127] = 127.0
+    return x.astype(np.float32)
+
+
+# -- activation quantization ------------------------------------------------------
+
+@pytest.mark.parametrize("kind", ["normal", "student_t", "wide", "edge"])
+@pytest.mark.parametrize("N,K", [(1, 4096), (4, 2048), (8, 256), (3, 8192)])
+def test_quantize_bit_exact(g, kind, N, K):
+    x = _inputs(kind, N, K, seed=N * K)
+    q, d = g.rfp2_quantize_act(dev(x))
+    qo, do = oracle.quantize_act(x)
+    np.testing.assert_array_equal(host(d), do)
+    np.testing.assert_array_equal(host(q), qo)
+
+
+# -- packers ------------------------------------------------------------------------
+
+def _weights(kind, M, K, seed=0):
+    rng = np.random.default_rng(seed)
+    if kind == "normal":
+        W = rng.normal(0, 0.02, (M, K))
+    elif kind == "student_t":
+        W = rng.standard_t(5, (M, K)) * 0.02
+        W[:, rng.choice(K, max(1, K // 100), replace=False)] *= 8
+    elif kind == "tiny":
+        W = rng.normal(0, 1e-5, (M, K))
+    elif kind == "huge":
+        W = rng.normal(0, 100.0, (M, K))
+    else:
+        W = rng.normal(0, 0.5, (M, K)) * (rng.random((M, K)) < 0.3)
+        W[0, :32] = 0.0
+        W[1, :32] = -0.0
+    return W.astype(np.float32)
+
+
+@pytest.mark.parametrize("kind", ["normal", "student_t", "tiny", "huge", "sparse"])
+def test_rfp2_pack_bit_exact(g, kind):
+    W = _weights(kind, 64, 512, seed=3)
+    P = host(g.rfp2_pack_weights(dev(W)))
+    np.testing.assert_array_equal(P, oracle.rfp2_pack(W))
+
+
+def test_rfp2_pack_tiny_config_bit_exact(g):
+    W = tiny_gemv()["W"]   # 256 x 1024, seed 0
+    np.testing.assert_array_equal(host(g.rfp2_pack_weights(dev(W))), oracle.rfp2_pack(W))
+
+
+@pytest.mark.parametrize("kind", ["normal", "student_t", "tiny", "huge", "sparse"])
+def test_hfp4_pack_bit_exact(g, kind):
+    W = _weights(kind, 48, 1024, seed=5)
+    st = status_tensor()
+    P = host(g.hfp4_pack_weights(dev(W), dev_status=st))
+    assert host(st)[0] == 0
+    np.testing.assert_array_equal(P, oracle.hfp4_pack(W))
+
+
+# -- int32 half sums ------------------------------------------------------------------
+
+def test_half_partials_bit_exact(g):
+    w = tiny_gemv(M=96, K=512, N=5, seed=7)
+    P = oracle.rfp2_pack(w["W"])
+    q, _ = oracle.quantize_act(w["x"])
+    got = host(g.rfp2_debug_half_partials(dev(P), 96, 512, dev(q)))
+    np.testing.assert_array_equal(got, oracle.rfp2_half_partials(P, 96, 512, q))
+
+
+def test_half_partials_extremes_bit_exact(g):
+    # +-127 activations against all-outer levels reach |S| = 16*4*127
+    rng = np.random.default_rng(1)
+    P = rng.integers(0, 256, (8, 4, 10)).astype(np.uint8)
+    P[:, :, 8:] = rng.integers(0, 0x7F, (8, 4, 2))
+    P[0, :, :8] = 0xFF
+    P[1, :, :8] = 0x00
+    q = rng.integers(-127, 128, (3, 128)).astype(np.int8)
+    q[0] = 127
+    q[1] = -127
+    got = host(g.rfp2_debug_half_partials(dev(P), 8, 128, dev(q)))
+    ref = oracle.rfp2_half_partials(P, 8, 128, q)
+    np.testing.assert_array_equal(got, ref)
+    assert np.abs(ref).max() == 16 * 4 * 127
+
+
+# -- dense GEMV ------------------------------------------------------------------------
+
+def _gemv_case(g, M, K, N, seed, fused=True):
+    rng = child_rngs(seed, 2)
+    W = normal_weights(rng[0], M, K, 0.02)
+    x = rng[1].standard_normal((N, K)).astype(np.float32)
+    P = oracle.rfp2_pack(W)
+    q, d = oracle.quantize_act(x)
+    ref = oracle.rfp2_gemv(P, M, K, q, d)
+    st = status_tensor()
+    if fused:
+        import torch
+        ws = torch.empty(g.rfp2_gemv_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
+        y = host(g.rfp2_gemv(dev(P), M, K, dev(x), workspace=ws, dev_status=st))
+        wsh = host(ws)
+        np.testing.assert_array_equal(wsh[:N * K].view(np.int8).reshape(N, K), q)
+        off = (N * K + 255) // 256 * 256
+        np.testing.assert_array_equal(wsh[off:off + N * K // 32 * 4].view(np.float32).reshape(N, -1), d)
+    else:
+        y = host(g.rfp2_gemv_q8(dev(P), M, K, dev(q), dev(d), dev_status=st))
+    assert host(st)[0] == 0
+    return y, ref
+
+
+@pytest.mark.parametrize("M,K,N", [
+    (256, 1024, 1), (1000, 4096, 1), (1000, 4096, 4), (777, 2048, 3), (64, 256, 8),
+    (333, 8192, 2), (50, 5120, 4), (130, 768, 5), (300, 1536, 6), (129, 2048, 7),
+    (1, 4096, 8), (5, 256, 1), (2048, 4096, 2),
+])
+def test_gemv_parity(g, M, K, N):
+    y, ref = _gemv_case(g, M, K, N, seed=M + K + N)
+    err = rel_err_rows(y, ref)
+    assert np.all(err <= TOL), err.max()
+
+
+@pytest.mark.parametrize("M,K,N", [(640, 4096, 1), (640, 4096, 4), (100, 2048, 8)])
+def test_gemv_q8_parity(g, M, K, N):
+    y, ref = _gemv_case(g, M, K, N, seed=11, fused=False)
+    assert np.all(rel_err_rows(y, ref) <= TOL)
+
+
+def test_gemv_max_k(g):
+    # K = 65536 at batch 1: every row spans all twelve consumer warps
+    y, ref = _gemv_case(g, 24, 65536, 1, seed=2)
+    assert np.all(rel_err_rows(y, ref) <= TOL)
+
+
+def test_gemv_tiny_config(g):
+    """256 x 1024 N(0, 0.02^2) weights, one N(0,1) vector, seed 0."""
+    w = tiny_gemv()
+    P = oracle.rfp2_pack(w["W"])
+    q, d = oracle.quantize_act(w["x"])
+    ref = oracle.rfp2_gemv(P, 256, 1024, q, d)
+    Pg = g.rfp2_pack_weights(dev(w["W"]))
+    np.testing.assert_array_equal(host(Pg), P)
+    y = host(g.rfp2_gemv(Pg, 256, 1024, dev(w["x"])))
+    assert np.all(rel_err_rows(y, ref) <= TOL)
+    # the brute-force fp64 formulation agrees too
+    assert np.all(rel_err_rows(y, oracle.rfp2_gemv_brute(P, 256, 1024, q, d)) <= TOL)
+
+
+@pytest.fixture(scope="module")
+def decode_full(g):
+    w = decode_gemv(N=4)   # 14336 x 4096, Student-t(5)*0.02, 41 outlier columns x8, seed 1
+    Pg = g.rfp2_pack_weights(dev(w["W"]))
+    return w, Pg
+
+
+@pytest.mark.parametrize("N", [1, 4])
+def test_decode_full_size_sampled(g, decode_full, N):
+    """Full 14336 x 4096 decode GEMV in the benchmark's launch configuration;
+    the oracle checks 96 sampled rows (packed bytes bit-exact, outputs within
+    tolerance normwise over the sample and elementwise against the sum of
+    absolute terms)."""
+    import torch
+    w, Pg = decode_full
+    M, K = w["W"].shape
+    rows = np.sort(np.random.default_rng(N).choice(M, 96, replace=False))
+    rows[0], rows[-1] = 0, M - 1
+    Po = oracle.rfp2_pack(w["W"][rows])
+    np.testing.assert_array_equal(host(Pg)[rows], Po)
+    x = w["x"][:N]
+    ws = torch.empty(g.rfp2_gemv_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
+    st = status_tensor()
+    y = host(g.rfp2_gemv(Pg, M, K, dev(x), workspace=ws, dev_status=st))
+    assert host(st)[0] == 0
+    q, d = oracle.quantize_act(x)
+    ref = oracle.rfp2_gemv(Po, len(rows), K, q, d)
+    assert np.all(rel_err_rows(y[:, rows], ref) <= TOL)
+    Wd = oracle.rfp2_decode(Po, len(rows), K).astype(np.float64)
+    a = q.astype(np.float64) * np.repeat(d.astype(np.float64), 32, axis=1)
+    bound = np.abs(a) @ np.abs(Wd).T
+    assert np.all(np.abs(y[:, rows] - ref) <= TOL * bound)
+    # properties that hold at any size: finite outputs everywhere
+    assert np.all(np.isfinite(y))
+
+
+def test_zero_inputs_give_exact_zero(g):
+    W = normal_weights(np.random.default_rng(0), 64, 512, 0.02)
+    P = oracle.rfp2_pack(W)
+    y = host(g.rfp2_gemv(dev(P), 64, 512, dev(np.zeros((2, 512), np.float32))))
+    assert np.all(y == 0.0)
+    Pz = oracle.rfp2_pack(np.zeros((16, 512), np.float32))
+    y = host(g.rfp2_gemv(dev(Pz), 16, 512, dev(np.ones((3, 512), np.float32))))
+    assert np.all(y == 0.0)
+
+
+def test_deterministic(g):
+    w = tiny_gemv(M=512, K=2048, N=4, seed=9)
+    P = dev(oracle.rfp2_pack(w["W"]))
+    y1 = host(g.rfp2_gemv(P, 512, 2048, dev(w["x"])))
+    y2 = host(g.rfp2_gemv(P, 512, 2048, dev(w["x"])))
+    np.testing.assert_array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
+def test_error_codes(g):
+    import torch
+    P = dev(np.zeros((8, 512 // 32, 10), np.uint8))
+    x = dev(np.zeros((1, 512), np.float32))
+    with pytest.raises(g.RFP2Error) as e:
+        g.rfp2_gemv(dev(np.zeros((8, 3, 10), np.uint8)), 8, 96, dev(np.zeros((1, 96), np.float32)))
+    assert e.value.status == 4   # K % 256 -> unsupported on the GPU
+    with pytest.raises(g.RFP2Error) as e:
+        g.rfp2_gemv(P, 8, 512, dev(np.zeros((9, 512), np.float32)))
+    assert e.value.status == 2   # N > 8
+    with pytest.raises(g.RFP2Error) as e:
+        g.rfp2_gemv(P, 8, 512, x, workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == 9   # workspace too small
+    raw = torch.zeros(8 * 160 + 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(g.RFP2Error) as e:
+        g.rfp2_gemv(raw[1:1 + 8 * 160], 8, 512, x)
+    assert e.value.status == 3   # weights not 16-byte aligned
+
+
+def test_validate_weights(g):
+    P = oracle.rfp2_pack(tiny_gemv(M=32, K=256)["W"])
+    st = status_tensor()
+    assert int(host(g.rfp2_validate_weights(dev(P), dev_status=st))[0]) == 0
+    assert host(st)[0] == 0
+    P[3, 2, 8] = 0x7F
+    P[7, 0, 9] = 0xC0
+    P[31, 7, 9] = 0xFF
+    bad = host(g.rfp2_validate_weights(dev(P), dev_status=st))
+    assert int(bad[0]) == 3 == oracle.rfp2_count_bad_scales(P)
+    assert host(st)[0] == 6   # RFP2_EBADSCALE
