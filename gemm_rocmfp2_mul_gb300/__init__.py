@@ -20,6 +20,7 @@ import threading
 __all__ = [
     "RFP2Error", "build", "lib", "library_path", "status_str",
     "rfp2_quantize_act", "rfp2_gemv_q8", "rfp2_gemv", "rfp2_gemv_workspace_bytes",
+    "rfp2_gemv_noalloc",
     "rfp2_moe_gemv", "rfp2_moe_workspace_bytes", "rfp2_gemm", "rfp2_gemm_workspace_bytes",
     "hfp4_gemv", "rfp2_pack_weights", "hfp4_pack_weights", "rfp2_validate_weights",
     "rfp2_debug_half_partials", "rfp2_row_bytes", "hfp4_row_bytes",
@@ -56,6 +57,7 @@ _SIGNATURES = {
     "rfp2_gemv_q8": (_I32, [_P, _I64, _I64, _P, _P, _I64, _P, _P, _P]),
     "rfp2_gemv_workspace_bytes": (_SZ, [_I64, _I64]),
     "rfp2_gemv": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
+    "rfp2_gemv_noalloc": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _P]),
     "rfp2_moe_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "rfp2_moe_gemv": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _P, _SZ, _P, _P]),
     "rfp2_gemm_workspace_bytes": (_SZ, [_I64, _I64]),
@@ -188,6 +190,21 @@ def rfp2_gemv(W, M, K, x, y=None, workspace=None, dev_status=None):
     ws = _workspace(workspace, nb, x)
     _check(lib().rfp2_gemv(_ptr(W), M, K, _ptr(x), N, _ptr(y), _ptr(ws), ws.numel(),
                            _ptr(dev_status), _stream()), "rfp2_gemv")
+    return y
+
+
+def rfp2_gemv_noalloc(W, M, K, x, y=None, dev_status=None):
+    """rfp2_gemv for callers that cannot allocate device memory: the quantized
+    activations go to scratch built into the library (N*K <= 65536; calls on
+    one device must not overlap on the GPU).  y fp32 [N, M]; pass `y` to avoid
+    the one torch allocation this wrapper would otherwise make."""
+    torch = _torch()
+    _need(W, torch.uint8, "W")
+    _need(x, torch.float32, "x")
+    N = x.shape[0]
+    y = _empty((N, M), torch.float32, x) if y is None else _need(y, torch.float32, "y")
+    _check(lib().rfp2_gemv_noalloc(_ptr(W), M, K, _ptr(x), N, _ptr(y), _ptr(dev_status),
+                                   _stream()), "rfp2_gemv_noalloc")
     return y
 
 

@@ -315,3 +315,71 @@ extern "C" rfp2_status rfp2_gemv(const uint8_t *W, int64_t M, int64_t K, const f
     if (e != cudaSuccess) return RFP2_ECUDA;
     return from_cuda(launch_gemv(W, M, K, q, d, N, y, dev_status, s, true));
 }
+
+// ---------------------------------------------------------------------------
+// rfp2_gemv_noalloc: rfp2_gemv for callers that cannot allocate device
+// memory.  Some callers run where a cudaMalloc is not allowed or not
+// possible: a plugin inside another runtime that owns the device memory
+// pool, code running under a memory budget that must not grow, or a path that
+// has to work after the pool is exhausted.  For them the quantized
+// activations (the only scratch rfp2_gemv needs) live in a fixed array in
+// device global memory that belongs to the library: every GPU that loads the
+// library holds it until the process exits.  The array is shared by every
+// call on a device, so calls that overlap on the GPU (different streams,
+// different host threads) race on it and must be serialized by the caller.
+// Nothing in it needs to start at zero: each call overwrites the part it uses.
+
+namespace rfp2 {
+namespace {
+
+// q int8 [N, K] (N*K <= kNoAllocMaxNK bytes) followed by d fp32 [N, K/32].
+constexpr int64_t kNoAllocMaxNK = 65536;
+constexpr size_t kNoAllocQBytes = kNoAllocMaxNK;
+constexpr size_t kNoAllocBytes = kNoAllocQBytes + kNoAllocMaxNK / 32 * sizeof(float);
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
+
+// Device address of the array, looked up once per device with that device
+// current (in host code the array's name is only a host-side stand-in).
+uint8_t *noalloc_scratch_ptr(int dev, cudaError_t *err) {
+    static std::mutex mu;
+    static uint8_t *ptrs[64] = {nullptr};
+    if (dev < 0 || dev >= 64) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) {
+            *err = e;
+            return nullptr;
+        }
+        ptrs[dev] = static_cast<uint8_t *>(p);
+    }
+    *err = cudaSuccess;
+    return ptrs[dev];
+}
+
+}  // namespace
+}  // namespace rfp2
+
+extern "C" rfp2_status rfp2_gemv_noalloc(const uint8_t *W, int64_t M, int64_t K, const float *x,
+                                         int64_t N, float *y, int32_t *dev_status,
+                                         rfp2_stream_t stream) {
+    if (!W || !x || !y) return RFP2_EINVAL;
+    if (M <= 0 || K <= 0 || N < 1 || N > RFP2_MAX_BATCH) return RFP2_ESHAPE;
+    if (N * K > kNoAllocMaxNK) return RFP2_EWORKSPACE;  // beyond the built-in scratch
+    const rfp2_status st = check_gemv_shape(M, K, N);
+    if (st != RFP2_OK) return st;
+    if (!aligned(W, 16) || !aligned(x, 4) || !aligned(y, 4)) return RFP2_EALIGN;
+    cudaError_t e = cudaSuccess;
+    uint8_t *scratch = noalloc_scratch_ptr(current_device(), &e);
+    if (!scratch) return RFP2_ECUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int8_t *q = reinterpret_cast<int8_t *>(scratch);
+    float *d = reinterpret_cast<float *>(scratch + kNoAllocQBytes);
+    e = launch_quantize(x, N, K, q, d, s, true);
+    if (e != cudaSuccess) return RFP2_ECUDA;
+    return from_cuda(launch_gemv(W, M, K, q, d, N, y, dev_status, s, true));
+}

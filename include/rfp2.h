@@ -120,6 +120,25 @@ rfp2_status rfp2_gemv(const uint8_t *W, int64_t M, int64_t K, const float *x, in
                       rfp2_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * rfp2_gemv without any device allocation by anyone.  The pages have no
+ * counterpart of this call: it exists for callers that cannot allocate device
+ * memory (a plugin whose host runtime owns the memory pool, a process under a
+ * fixed memory budget, a path that must work after the pool ran out) and so
+ * cannot pass rfp2_gemv a workspace.  Same inputs, outputs and result as
+ * rfp2_gemv; the quantized activations go to a fixed scratch array inside the
+ * library (73,728 bytes of device memory, held on every GPU that loads the
+ * library until the process exits).  Limits: N * K <= 65536; larger sizes
+ * return RFP2_EWORKSPACE.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  All calls on a device share the array: calls that overlap
+ * on the GPU race on it, so the caller serializes them.  Nothing in the array
+ * needs clearing; every call overwrites what it uses.
+ * Errors: as rfp2_gemv_q8, plus EWORKSPACE (N * K too large).
+ */
+rfp2_status rfp2_gemv_noalloc(const uint8_t *W, int64_t M, int64_t K, const float *x, int64_t N,
+                              float *y, int32_t *dev_status, rfp2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * MoE bulk-expert GEMV (MUL_MAT_ID over the routed experts' rows for a few
  * tokens: "HRX on the Radeon iGPU", section "MoE decode and the kernel
  * cache").
