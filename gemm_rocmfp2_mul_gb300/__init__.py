@@ -22,7 +22,7 @@ __all__ = [
     "rfp2_quantize_act", "rfp2_gemv_q8", "rfp2_gemv", "rfp2_gemv_workspace_bytes",
     "rfp2_gemv_noalloc",
     "rfp2_moe_gemv", "rfp2_moe_workspace_bytes", "rfp2_gemm", "rfp2_gemm_workspace_bytes",
-    "hfp4_gemv", "rfp2_pack_weights", "hfp4_pack_weights", "rfp2_validate_weights",
+    "hfp4_gemv", "hfp4_gemv_workspace_bytes", "rfp2_pack_weights", "hfp4_pack_weights", "rfp2_validate_weights",
     "rfp2_debug_half_partials", "rfp2_row_bytes", "hfp4_row_bytes",
 ]
 
@@ -62,7 +62,8 @@ _SIGNATURES = {
     "rfp2_moe_gemv": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _P, _SZ, _P, _P]),
     "rfp2_gemm_workspace_bytes": (_SZ, [_I64, _I64]),
     "rfp2_gemm": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
-    "hfp4_gemv": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _P]),
+    "hfp4_gemv_workspace_bytes": (_SZ, [_I64, _I64]),
+    "hfp4_gemv": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
     "rfp2_pack_weights": (_I32, [_P, _I64, _I64, _P, _P]),
     "hfp4_pack_weights": (_I32, [_P, _I64, _I64, _P, _P, _P]),
     "rfp2_validate_weights": (_I32, [_P, _I64, _P, _P, _P]),
@@ -247,15 +248,20 @@ def rfp2_gemm(W, M, K, X, Y=None, workspace=None, dev_status=None):
     return Y
 
 
-def hfp4_gemv(W, M, K, x, y=None, dev_status=None):
+def hfp4_gemv_workspace_bytes(N: int, K: int) -> int:
+    return int(lib().hfp4_gemv_workspace_bytes(N, K))
+
+
+def hfp4_gemv(W, M, K, x, y=None, workspace=None, dev_status=None):
     """HFP4G32 GEMV: y fp32 [N, M]."""
     torch = _torch()
     _need(W, torch.uint8, "W")
     _need(x, torch.float32, "x")
     N = x.shape[0]
     y = _empty((N, M), torch.float32, x) if y is None else _need(y, torch.float32, "y")
-    _check(lib().hfp4_gemv(_ptr(W), M, K, _ptr(x), N, _ptr(y), _ptr(dev_status), _stream()),
-           "hfp4_gemv")
+    ws = _workspace(workspace, hfp4_gemv_workspace_bytes(N, K), x)
+    _check(lib().hfp4_gemv(_ptr(W), M, K, _ptr(x), N, _ptr(y), _ptr(ws), ws.numel(),
+                           _ptr(dev_status), _stream()), "hfp4_gemv")
     return y
 
 

@@ -2,8 +2,40 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace rfp2 {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (so the
+// library does not link libcuda itself).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode_tensor_map_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
+                          uint64_t cols, uint64_t rows, uint64_t row_bytes, uint32_t box_cols,
+                          uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t elem_strides[2] = {1, 1};
+    const CUresult r = fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, elem_strides,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
 
 int current_device() {
     int dev = 0;

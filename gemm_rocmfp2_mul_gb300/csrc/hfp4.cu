@@ -1,0 +1,370 @@
+// HFP4G32 GEMV: y[n, m] = row_scale_a(m) * sum_b 2^(e_b - 127) *
+// sum_i E2M1[c_i] * x[n, 32b + i], fp32 activations, fp32 accumulation.
+//
+// Source: "HFP4" (hipfire.dev), sections "Element format (OCP E2M1)",
+// "Block scale - UE8M0", "Per-row second-level scale (FP16)" (row_scale_a is
+// applied once per row, outside the K loop), "Byte layout - HFP4G32" and
+// "Nibble packing"; the page's correctness-anchor loop is the oracle.
+//
+// GB300 design (the page's kernels are RDNA v_ldexp/WMMA code):
+//  * E2M1 codes are exact in f16, so each 32-weight block is one pair of
+//    m16n8k16 f16 MMAs per row tile with a fresh fp32 accumulator, scaled by
+//    2^(e-127) in the epilogue (the block exponent varies per row and block,
+//    so it cannot be folded into the accumulation).  The N <= 8 activation
+//    columns are the MMA's n dimension, so the weight decode (one E2M1x2 ->
+//    f16x2 conversion per two weights) is shared by all columns.
+//  * fp32 activations are made exact enough for f16 by a prep kernel: each
+//    column is scaled by a power of two 2^-kc (max |x| -> [1, 2)) and split
+//    into two f16 pieces x' ~= hi + lo (relative residual <= 2^-22); both
+//    pieces go through the MMA, and 2^kc is applied with row_scale_a at the
+//    end.  The prep kernel writes the pieces in MMA fragment order.
+//  * Weights stream through 2-D TMA tiles of 64 rows x 1024 K (544 bytes per
+//    row; rows past M and columns past the row are zero-filled), with the
+//    matching activation fragments, into a 3-4 stage ring; eight consumer
+//    warps each take 4 of the 32 blocks of a tile, and their partial sums are
+//    combined in shared memory.  All waits are bounded.
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "tma.cuh"
+
+namespace rfp2 {
+namespace {
+
+constexpr int kTile = 16;                // MMA rows
+constexpr int kMaxTiles = 4;             // row tiles per CTA
+constexpr int kRows = kTile * kMaxTiles; // 64 rows per stage
+constexpr int kChunkBlocks = 32;         // 1024 K per stage
+constexpr int kChunkRowBytes = kChunkBlocks * 17;  // 544
+constexpr int kWStageBytes = kRows * kChunkRowBytes;  // 34816
+constexpr int kWarps = 8;                // consumer warps, 4 blocks each
+constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kRedBytes = kWarps * kMaxTiles * 32 * 16;
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// workspace: kc int32 [N] (256 bytes) then fragments uint4 [K/16][N][4]
+size_t hfp4_ws_bytes(int64_t N, int64_t K) { return 256 + (size_t)(K / 16) * N * 4 * 16; }
+
+__device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
+    return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+}
+
+// One CTA per activation column: power-of-two scaling and the two-piece f16
+// split, written in the B-fragment order of mma.m16n8k16 for the K
+// permutation used by the GEMV (MMA k 2p+i <-> element 8p+4s+i and
+// 2p+8+i <-> 8p+4s+2+i of a 32-element block, k-step s of the block).
+__global__ void __launch_bounds__(256) hfp4_split_kernel(const float *__restrict__ x, int N, int K,
+                                                         int *kc_out, uint4 *frag) {
+    __shared__ float wmax[8];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int n = blockIdx.x;
+    const float *xr = x + (int64_t)n * K;
+    float amax = 0.0f;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) amax = fmaxf(amax, fabsf(xr[k]));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = 0.0f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, wmax[i]);
+    const int kc = amax > 0.0f ? ilogbf(amax) : 0;  // max |x| * 2^-kc in [1, 2)
+    if (threadIdx.x == 0) kc_out[n] = kc;
+    const int entries = (K / 16) * 4;
+    for (int e = threadIdx.x; e < entries; e += blockDim.x) {
+        const int ks = e >> 2, p = e & 3;
+        const int base = (ks >> 1) * 32 + 8 * p + 4 * (ks & 1);
+        __half h1[4], h2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float v = ldexpf(xr[base + i], -kc);
+            h1[i] = __float2half_rn(v);
+            h2[i] = __float2half_rn(v - __half2float(h1[i]));
+        }
+        frag[((int64_t)ks * N + n) * 4 + p] =
+            make_uint4(pack_h2(h1[0], h1[1]), pack_h2(h1[2], h1[3]), pack_h2(h2[0], h2[1]),
+                       pack_h2(h2[2], h2[3]));
+    }
+}
+
+// Two E2M1 codes (low nibble = even element) -> f16x2 (low half = even).
+__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
+    uint32_t h;
+    asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(h) : "r"(byte));
+    return h;
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// UE8M0 byte -> 2^(e-127) as fp32 (e = 0 is the subnormal 2^-127, 0xFF NaN).
+__device__ __forceinline__ float ue8m0(uint32_t e) {
+    uint32_t bits = e << 23;
+    bits = e == 0 ? 0x00400000u : bits;
+    bits = e == 0xFF ? 0x7FC00000u : bits;
+    return __uint_as_float(bits);
+}
+
+// Four bytes of a row starting at an arbitrary byte address in shared memory.
+__device__ __forceinline__ uint32_t load_u32_unaligned(const uint8_t *p) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(a & ~uintptr_t(3));
+    return __funnelshift_r(w[0], w[1], (uint32_t)(a & 3) * 8);
+}
+
+struct HfpArgs {
+    const uint8_t *W;
+    int M, K, N, rb;
+    int tiles_per_cta, tiles_extra, nstages;
+    float *y;
+    int32_t *status;
+    const int *kc;
+    const uint4 *frag;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    hfp4_gemv_kernel(const __grid_constant__ CUtensorMap wmap, HfpArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int S = a.nstages;
+    const int bstage_bytes = 64 * a.N * 64;  // 64 k-steps x N columns x 4 lanes x 16 B
+    uint8_t *wst = smem;                                        // [S][kWStageBytes]
+    uint8_t *bst = smem + (size_t)S * kWStageBytes;             // [S][bstage_bytes]
+    float *red = reinterpret_cast<float *>(bst + (size_t)S * bstage_bytes);  // [8][4][32][4]
+    uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(red) + kRedBytes);
+    uint64_t *empty = full + S;
+    uint64_t *red_bar = empty + S;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(red_bar + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bx = blockIdx.x;
+    const int tile0 = bx * a.tiles_per_cta + min(bx, a.tiles_extra);
+    const int ntiles = a.tiles_per_cta + (bx < a.tiles_extra ? 1 : 0);
+    const int row0 = tile0 * kTile;
+    const int KB = a.K >> 5;
+    const int nchunks = (KB + kChunkBlocks - 1) / kChunkBlocks;
+    const int nks = a.K / 16;
+
+    if (threadIdx.x == kWarps * 32) {
+        prefetch_tensor_map(&wmap);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
+        }
+        mbar_init(red_bar, kWarps);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kWarps) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int c = 0;
+            // the weight tiles do not depend on earlier kernels: start them first
+            for (; c < nchunks && c < S; ++c) {
+                const int ks0 = c * 2 * kChunkBlocks;
+                const int bbytes = min(2 * kChunkBlocks, nks - ks0) * a.N * 64;
+                mbar_arrive_expect_tx(&full[c], kWStageBytes + bbytes);
+                tma_load_2d_hint(wst + (size_t)c * kWStageBytes, &wmap, 4 + c * (kChunkRowBytes / 4),
+                                 row0, &full[c], pol);
+            }
+            pdl_wait();  // the activation fragments come from the split kernel
+            for (int i = 0; i < c; ++i) {
+                const int ks0 = i * 2 * kChunkBlocks;
+                const int bbytes = min(2 * kChunkBlocks, nks - ks0) * a.N * 64;
+                bulk_g2s(bst + (size_t)i * bstage_bytes, a.frag + (int64_t)ks0 * a.N * 4, bbytes,
+                         &full[i]);
+            }
+            for (; c < nchunks; ++c) {
+                const int s = c % S;
+                if (!mbar_wait(&empty[s], ((c / S) - 1) & 1)) {
+                    record_status(a.status, RFP2_ETIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                const int ks0 = c * 2 * kChunkBlocks;
+                const int bbytes = min(2 * kChunkBlocks, nks - ks0) * a.N * 64;
+                mbar_arrive_expect_tx(&full[s], kWStageBytes + bbytes);
+                tma_load_2d_hint(wst + (size_t)s * kWStageBytes, &wmap, 4 + c * (kChunkRowBytes / 4),
+                                 row0, &full[s], pol);
+                bulk_g2s(bst + (size_t)s * bstage_bytes, a.frag + (int64_t)ks0 * a.N * 4, bbytes,
+                         &full[s]);
+            }
+            for (int i = max(0, c - S); i < c; ++i)
+                if (!mbar_wait(&full[i % S], (i / S) & 1)) record_status(a.status, RFP2_ETIMEOUT);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------------ consumers
+    pdl_wait();
+    pdl_launch_dependents();
+    const int g = lane >> 2, p = lane & 3;
+    float acc[kMaxTiles][4];
+#pragma unroll
+    for (int t = 0; t < kMaxTiles; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
+        const int s = c % S;
+        if (*abort_flag || !mbar_wait(&full[s], (c / S) & 1)) {
+            record_status(a.status, RFP2_ETIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+        }
+        const uint8_t *ws = wst + (size_t)s * kWStageBytes;
+        const uint4 *bs = reinterpret_cast<const uint4 *>(bst + (size_t)s * bstage_bytes);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int j = warp * 4 + jj;  // block inside the chunk
+            if (c * kChunkBlocks + j >= KB) break;
+            uint4 b0 = make_uint4(0, 0, 0, 0), b1 = make_uint4(0, 0, 0, 0);
+            if (g < a.N) {
+                b0 = bs[((2 * j) * a.N + g) * 4 + p];
+                b1 = bs[((2 * j + 1) * a.N + g) * 4 + p];
+            }
+#pragma unroll
+            for (int t = 0; t < kMaxTiles; ++t) {
+                if (t < ntiles) {
+                    const uint8_t *ra = ws + (t * kTile + g) * kChunkRowBytes + j * 17;
+                    const uint8_t *rbp = ra + 8 * kChunkRowBytes;
+                    const uint32_t wa = load_u32_unaligned(ra + 1 + 4 * p);
+                    const uint32_t wb = load_u32_unaligned(rbp + 1 + 4 * p);
+                    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    // k-step 0: bytes 0,1 of the word; k-step 1: bytes 2,3
+                    const uint32_t a0 = e2m1x2_to_h2(wa), a1 = e2m1x2_to_h2(wb);
+                    const uint32_t a2 = e2m1x2_to_h2(wa >> 8), a3 = e2m1x2_to_h2(wb >> 8);
+                    mma_f16(d, a0, a1, a2, a3, b0.x, b0.y);
+                    mma_f16(d, a0, a1, a2, a3, b0.z, b0.w);
+                    const uint32_t a4 = e2m1x2_to_h2(wa >> 16), a5 = e2m1x2_to_h2(wb >> 16);
+                    const uint32_t a6 = e2m1x2_to_h2(wa >> 24), a7 = e2m1x2_to_h2(wb >> 24);
+                    mma_f16(d, a4, a5, a6, a7, b1.x, b1.y);
+                    mma_f16(d, a4, a5, a6, a7, b1.z, b1.w);
+                    const float sa = ue8m0(ra[0]), sb = ue8m0(rbp[0]);
+                    acc[t][0] = fmaf(d[0], sa, acc[t][0]);
+                    acc[t][1] = fmaf(d[1], sa, acc[t][1]);
+                    acc[t][2] = fmaf(d[2], sb, acc[t][2]);
+                    acc[t][3] = fmaf(d[3], sb, acc[t][3]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // combine the eight K-slices: every warp writes its partials, warp 0 sums
+    float4 *red4 = reinterpret_cast<float4 *>(red);
+#pragma unroll
+    for (int t = 0; t < kMaxTiles; ++t)
+        red4[(warp * kMaxTiles + t) * 32 + lane] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(red_bar);
+    if (warp != 0) return;
+    if (!mbar_wait(red_bar, 0)) {
+        record_status(a.status, RFP2_ETIMEOUT);
+        return;
+    }
+    if (!ok) return;
+    const int c0 = 2 * p, c1 = 2 * p + 1;
+    const float s0 = c0 < a.N ? ldexpf(1.0f, a.kc[c0]) : 0.0f;
+    const float s1 = c1 < a.N ? ldexpf(1.0f, a.kc[c1]) : 0.0f;
+    for (int t = 0; t < ntiles; ++t) {
+        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int w = 0; w < kWarps; ++w) {
+            const float4 q = red4[(w * kMaxTiles + t) * 32 + lane];
+            v[0] += q.x;
+            v[1] += q.y;
+            v[2] += q.z;
+            v[3] += q.w;
+        }
+        const int r0 = row0 + t * kTile + g, r1 = r0 + 8;
+        if (r0 < a.M) {
+            const float rs = __half2float(*reinterpret_cast<const __half *>(a.W + (int64_t)r0 * a.rb));
+            if (c0 < a.N) a.y[(int64_t)c0 * a.M + r0] = v[0] * rs * s0;
+            if (c1 < a.N) a.y[(int64_t)c1 * a.M + r0] = v[1] * rs * s1;
+        }
+        if (r1 < a.M) {
+            const float rs = __half2float(*reinterpret_cast<const __half *>(a.W + (int64_t)r1 * a.rb));
+            if (c0 < a.N) a.y[(int64_t)c0 * a.M + r1] = v[2] * rs * s0;
+            if (c1 < a.N) a.y[(int64_t)c1 * a.M + r1] = v[3] * rs * s1;
+        }
+    }
+}
+
+}  // namespace
+}  // namespace rfp2
+
+using namespace rfp2;
+
+extern "C" size_t hfp4_gemv_workspace_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0) return 0;
+    return hfp4_ws_bytes(N, K);
+}
+
+extern "C" rfp2_status hfp4_gemv(const uint8_t *W, int64_t M, int64_t K, const float *x, int64_t N,
+                                 float *y, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, rfp2_stream_t stream) {
+    if (!W || !x || !y) return RFP2_EINVAL;
+    if (M <= 0 || K <= 0 || N < 1 || N > RFP2_MAX_BATCH) return RFP2_ESHAPE;
+    if (M > (1 << 30) || K > (1 << 24)) return RFP2_ESHAPE;
+    if (K % 512 != 0) return RFP2_EUNSUPPORTED;  // rows must be whole 16-byte units
+    if (!workspace || workspace_bytes < hfp4_ws_bytes(N, K)) return RFP2_EWORKSPACE;
+    if (!aligned(W, 16) || !aligned(x, 4) || !aligned(y, 4) || !aligned(workspace, 256))
+        return RFP2_EALIGN;
+    const int rb = (int)(16 + 17 * (K / 32));
+    CUtensorMap wmap;
+    if (!encode_tensor_map_2d(&wmap, W, CU_TENSOR_MAP_DATA_TYPE_UINT32, (uint64_t)rb / 4,
+                              (uint64_t)M, (uint64_t)rb, kChunkRowBytes / 4, kRows))
+        return RFP2_ECUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int *kc = static_cast<int *>(workspace);
+    uint4 *frag = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(workspace) + 256);
+    cudaError_t e = launch(hfp4_split_kernel, dim3((unsigned)N), dim3(256), 0, s, true, x, (int)N,
+                           (int)K, kc, frag);
+    if (e != cudaSuccess) return RFP2_ECUDA;
+    // stages: as many 64-row x 1024-K tiles (plus their fragments) as fit
+    const size_t per_stage = kWStageBytes + (size_t)64 * N * 64;
+    int stages = 4;
+    while (stages > 2 && stages * per_stage + kRedBytes + 256 > 227 * 1024) --stages;
+    const size_t smem = stages * per_stage + kRedBytes + 256;
+    static std::mutex mu;
+    static int configured[64] = {0};
+    const int dev = current_device();
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && !configured[dev]) {
+            if (set_smem_limit(hfp4_gemv_kernel, 227 * 1024) != cudaSuccess) return RFP2_ECUDA;
+            configured[dev] = 1;
+        }
+    }
+    const int tiles = (int)((M + kTile - 1) / kTile);
+    int grid = sm_count(dev);
+    if (grid > tiles) grid = tiles;
+    while ((tiles + grid - 1) / grid > kMaxTiles) ++grid;
+    HfpArgs a;
+    a.W = W;
+    a.M = (int)M;
+    a.K = (int)K;
+    a.N = (int)N;
+    a.rb = rb;
+    a.tiles_per_cta = tiles / grid;
+    a.tiles_extra = tiles % grid;
+    a.nstages = stages;
+    a.y = y;
+    a.status = dev_status;
+    a.kc = kc;
+    a.frag = frag;
+    return from_cuda(launch(hfp4_gemv_kernel, dim3(grid), dim3(kThreads), smem, s, true, wmap, a));
+}

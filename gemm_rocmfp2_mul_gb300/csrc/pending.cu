@@ -1,13 +1,9 @@
-// Entry points whose kernels are not written yet: they return
-// RFP2_EUNSUPPORTED so the ABI is complete while the kernels land.
+// Entry point whose kernel is not written yet: it returns
+// RFP2_EUNSUPPORTED so the ABI is complete while the kernel lands.
 #include "common.cuh"
 
 extern "C" size_t rfp2_gemm_workspace_bytes(int64_t, int64_t) { return 0; }
 extern "C" rfp2_status rfp2_gemm(const uint8_t *, int64_t, int64_t, const uint16_t *, int64_t,
                                  float *, void *, size_t, int32_t *, rfp2_stream_t) {
-    return RFP2_EUNSUPPORTED;
-}
-extern "C" rfp2_status hfp4_gemv(const uint8_t *, int64_t, int64_t, const float *, int64_t,
-                                 float *, int32_t *, rfp2_stream_t) {
     return RFP2_EUNSUPPORTED;
 }

@@ -184,11 +184,17 @@ rfp2_status rfp2_gemm(const uint8_t *W, int64_t M, int64_t K, const uint16_t *X,
  * sum_b 2^(e_b - 127) * sum_i E2M1[c_i] * x[n, i], fp32 activations, fp32
  * accumulation, row scale applied once at the end of the row.
  *   W  uint8 [M, 16 + 17*K/32] device, 16-byte aligned; x fp32 [N, K];
- *   y fp32 [N, M] (output).  1 <= N <= RFP2_MAX_BATCH, K % 256 == 0.
- * Errors: EINVAL, ESHAPE, EUNSUPPORTED, EALIGN, ECUDA.
+ *   y fp32 [N, M] (output).  1 <= N <= RFP2_MAX_BATCH, K % 512 == 0 (a row
+ *   is then a whole number of 16-byte units).
+ *   workspace: hfp4_gemv_workspace_bytes(N, K) bytes, 256-byte aligned (the
+ *   activations split into two fp16 pieces in tensor-core fragment order).
+ * A block byte 0xFF (block NaN) gives NaN in the affected outputs.
+ * Errors: EINVAL, ESHAPE, EUNSUPPORTED (K % 512), EALIGN, EWORKSPACE, ECUDA.
  */
+size_t hfp4_gemv_workspace_bytes(int64_t N, int64_t K);
 rfp2_status hfp4_gemv(const uint8_t *W, int64_t M, int64_t K, const float *x, int64_t N,
-                      float *y, int32_t *dev_status, rfp2_stream_t stream);
+                      float *y, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                      rfp2_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Weight packers (offline preparation; "02 Quantization" for ROCmFP2 and
