@@ -1,0 +1,230 @@
+// Prefill GEMM on the 5th-generation tensor cores:
+// Y[n, m] = sum_k X[n, k] * w[m, k], X bf16 [N, K] (tokens), w the ROCmFP2
+// weights [M, K] expanded exactly to bf16, Y fp32 [N, M].
+//
+// Source: "ROCmFP2 codebook research report", sections "02 Quantization"
+// (weight = codebook[code] * UE4M3 scale: at most 4 significant bits times a
+// power of two, hence exact in bf16) and "04 Measured evidence" (the
+// end-to-end gain of the format comes from prefill, a dense contraction).
+//
+// Two launches:
+//  1. expand: packed 10-byte blocks -> bf16 rows in the workspace (one thread
+//     per 32-weight block, 64 bytes written per block).
+//  2. gemm: one CTA per 128-token x 256-weight-row tile.  Warp 0 loads
+//     K-major 64-element slices of both operands with 2-D TMA (SWIZZLE_128B)
+//     into a 4-stage ring; one thread of warp 1 issues tcgen05.mma kind::f16
+//     (M=128, N=256, K=16, bf16 in, fp32 accumulate in tensor memory) and
+//     frees each stage with tcgen05.commit; warps 2-5 read the 128 x 256
+//     accumulator back with tcgen05.ld (each warp its 32-lane quarter) and
+//     store fp32 rows.  Every wait is bounded; tensor memory is always freed.
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "rfp2_decode.cuh"
+#include "tcgen05.cuh"
+#include "tma.cuh"
+
+namespace rfp2 {
+namespace {
+
+constexpr int BM = 128;  // tokens per tile (UMMA M)
+constexpr int BN = 256;  // weight rows per tile (UMMA N)
+constexpr int BK = 64;   // K per stage: one 128-byte swizzle row
+constexpr int UK = 16;   // K per UMMA instruction
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;
+constexpr int kBBytes = BN * BK * 2;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kThreads = 6 * 32;
+constexpr uint32_t kTmemCols = 256;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
+
+// ---- expand ----------------------------------------------------------------
+__global__ void __launch_bounds__(256) expand_bf16_kernel(const uint8_t *__restrict__ W,
+                                                          int64_t nblocks,
+                                                          __nv_bfloat16 *__restrict__ out) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= nblocks) return;
+    const uint8_t *b = W + j * 10;
+    uint32_t lo = b[0] | (b[1] << 8) | (b[2] << 16) | ((uint32_t)b[3] << 24);
+    uint32_t hi = b[4] | (b[5] << 8) | (b[6] << 16) | ((uint32_t)b[7] << 24);
+    float s0, s1;
+    decode_scale_pair((uint32_t)b[8] | ((uint32_t)b[9] << 8), s0, s1);
+    const float lv[4] = {-4.0f, -1.0f, 1.0f, 4.0f};
+    uint4 *o = reinterpret_cast<uint4 *>(out + j * 32);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // 8 weights per 16-byte store
+        const uint32_t c = q < 2 ? lo >> (16 * q) : hi >> (16 * (q - 2));
+        const float s = q < 2 ? s0 : s1;
+        uint32_t v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat16 w0 = __float2bfloat16_rn(lv[(c >> (4 * i)) & 3] * s);
+            const __nv_bfloat16 w1 = __float2bfloat16_rn(lv[(c >> (4 * i + 2)) & 3] * s);
+            v[i] = (uint32_t)__bfloat16_as_ushort(w0) | ((uint32_t)__bfloat16_as_ushort(w1) << 16);
+        }
+        o[q] = make_uint4(v[0], v[1], v[2], v[3]);
+    }
+}
+
+// ---- GEMM --------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+                     float *__restrict__ Y, int Ntok, int Mw, int K, int32_t *status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kStages * kStageBytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *accum_bar = empty + kStages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum_bar + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile_m = blockIdx.x, tile_n = blockIdx.y;
+    const int nk = K / BK;
+
+    if (threadIdx.x == 0) {
+        prefetch_tensor_map(&xmap);
+        prefetch_tensor_map(&wmap);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accum_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---- TMA producer
+        pdl_wait();  // X and the expanded weights come from earlier kernels
+        int kb = 0;
+        for (; kb < nk; ++kb) {
+            const int s = kb % kStages;
+            if (kb >= kStages && !mbar_wait(&empty[s], ((kb / kStages) - 1) & 1)) {
+                record_status(status, RFP2_ETIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            if (*abort_flag) break;
+            uint8_t *a = smem + (size_t)s * kStageBytes;
+            mbar_arrive_expect_tx(&full[s], kStageBytes);
+            tma_load_2d(a, &xmap, kb * BK, tile_m * BM, &full[s]);
+            tma_load_2d(a + kABytes, &wmap, kb * BK, tile_n * BN, &full[s]);
+        }
+        // copies still in flight must land before the CTA retires
+        for (int i = max(0, kb - kStages); i < kb; ++i)
+            if (!mbar_wait(&full[i % kStages], (i / kStages) & 1)) record_status(status, RFP2_ETIMEOUT);
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % kStages;
+            if (*abort_flag || !mbar_wait(&full[s], (kb / kStages) & 1)) {
+                record_status(status, RFP2_ETIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a = smem_addr(smem + (size_t)s * kStageBytes);
+            const uint64_t adesc = smem_desc_sw128(a);
+            const uint64_t bdesc = smem_desc_sw128(a + kABytes);
+#pragma unroll
+            for (int k = 0; k < BK / UK; ++k)
+                umma_bf16(tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            umma_commit(&empty[s]);  // the stage is free once these MMAs complete
+        }
+        umma_commit(accum_bar);  // accumulator complete (or, after an abort, idle)
+    } else if (warp >= 2) {
+        // ---- epilogue: TMEM -> registers -> Y
+        const bool ok = mbar_wait(accum_bar, 0);
+        if (!ok) record_status(status, RFP2_ETIMEOUT);
+        tc_fence_after();
+        const int q = warp & 3;  // TMEM lanes 32q .. 32q+31
+        const int row = tile_m * BM + q * 32 + lane;
+        if (ok && !*abort_flag) {
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + c * 32, r);
+                tmem_ld_wait();
+                const int col0 = tile_n * BN + c * 32;
+                if (row < Ntok) {
+                    float4 *dst = reinterpret_cast<float4 *>(Y + (int64_t)row * Mw + col0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (col0 + 4 * i < Mw)
+                            dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                 __uint_as_float(r[4 * i + 2]),
+                                                 __uint_as_float(r[4 * i + 3]));
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+}  // namespace rfp2
+
+using namespace rfp2;
+
+extern "C" size_t rfp2_gemm_workspace_bytes(int64_t M, int64_t K) {
+    if (M <= 0 || K <= 0) return 0;
+    return (size_t)M * K * 2;
+}
+
+extern "C" rfp2_status rfp2_gemm(const uint8_t *W, int64_t M, int64_t K, const uint16_t *X,
+                                 int64_t N, float *Y, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, rfp2_stream_t stream) {
+    if (!W || !X || !Y) return RFP2_EINVAL;
+    if (M <= 0 || K <= 0 || N <= 0) return RFP2_ESHAPE;
+    if (M > (1LL << 30) || N > (1LL << 30) || K > (1 << 20)) return RFP2_ESHAPE;
+    if (K % 256 != 0 || M % 16 != 0) return RFP2_EUNSUPPORTED;
+    if (!workspace || workspace_bytes < (size_t)M * K * 2) return RFP2_EWORKSPACE;
+    if (!aligned(W, 16) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(workspace, 1024))
+        return RFP2_EALIGN;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    __nv_bfloat16 *wexp = static_cast<__nv_bfloat16 *>(workspace);
+    const int64_t nblocks = M * (K / 32);
+    cudaError_t e = launch(expand_bf16_kernel, dim3((unsigned)((nblocks + 255) / 256)), dim3(256),
+                           0, s, true, W, nblocks, wexp);
+    if (e != cudaSuccess) return RFP2_ECUDA;
+    CUtensorMap xmap, wmap;
+    if (!encode_tensor_map_2d(&xmap, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K, (uint64_t)N,
+                              (uint64_t)K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_2d(&wmap, wexp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K,
+                              (uint64_t)M, (uint64_t)K * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return RFP2_ECUDA;
+    static std::mutex mu;
+    static int configured[64] = {0};
+    const int dev = current_device();
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && !configured[dev]) {
+            if (set_smem_limit(gemm_bf16_kernel, (int)kSmemBytes) != cudaSuccess) return RFP2_ECUDA;
+            configured[dev] = 1;
+        }
+    }
+    const dim3 grid((unsigned)((N + BM - 1) / BM), (unsigned)((M + BN - 1) / BN));
+    return from_cuda(launch(gemm_bf16_kernel, grid, dim3(kThreads), kSmemBytes, s, true, xmap, wmap,
+                            Y, (int)N, (int)M, (int)K, dev_status));
+}
