@@ -122,6 +122,61 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# multi-rank aggregation (replicas: every rank runs the same workload)
+
+
+def max_over_ranks(value: float, device) -> float:
+    """Largest `value` over the ranks of the default process group (the
+    slowest replica's time), or `value` itself without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_step: int, ms_per_step_max: float, world: int) -> float:
+    """Whole-job throughput: the bytes all replicas processed per step over
+    the slowest replica's step time."""
+    return world * bytes_per_step / (ms_per_step_max * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------------------
+# ncu traffic figure (only while the kernel sources are those it was taken on)
+
+GEMV_SOURCES = ["gemv.cu", "gemv_core.cuh", "rfp2_decode.cuh", "common.cuh", "quantize.cu"]
+
+
+def gemv_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMV_SOURCES:
+        with open(os.path.join(ROOT, "gemm_rocmfp2_mul_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic():
+    """dram read+write bytes per GEMV launch from the committed ncu summary,
+    or None if the kernel sources changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "gemv_q8_decode_14336x4096_traffic.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_sha256") != gemv_source_hash():
+            return None
+        return int(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 
 
@@ -229,12 +284,9 @@ def run_gpu(args):
     torch.cuda.synchronize()
     t1 = time.time()
     total_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, "cuda")
     ms_per_step = total_ms / args.steps
-    value = world * WEIGHT_BYTES / (ms_per_step * 1e-3) / 1e9
+    value = aggregate_gbs(WEIGHT_BYTES, ms_per_step, world)
 
     # ---- the GEMV kernel alone (roofline) and batch 4
     kreps = max(1, 5000 // G)
@@ -246,6 +298,11 @@ def run_gpu(args):
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(torch, gl, w, Pc, copies, args.steps)
+    del Pc
+    torch.cuda.empty_cache()
+
+    # ---- the other rows of the hot path on their own workloads
+    sec = {} if args.no_secondary else secondary(torch, gl, peaks)
 
     achieved = WEIGHT_BYTES / (ms_k * 1e-3) / 1e9
     out = {
@@ -277,18 +334,19 @@ def run_gpu(args):
             "peak": peaks["hbm_gbs"],
             "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": args.traffic,
+            "traffic": args.traffic if args.traffic is not None else measured_traffic(),
             "peak_source": peaks["source"] + " hbm_gbs",
             "us_per_launch": round(ms_k * 1e3, 3),
         },
-        "secondary": {
+        "secondary": dict({
             "decode_batch4": {
-                "GB_per_s": round(WEIGHT_BYTES / (ms_b4 * 1e-3) / 1e9, 1),
+                "workload": "same weights, batch 4 (activation quantize fused)",
+                "value": round(WEIGHT_BYTES / (ms_b4 * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "us_per_call": round(ms_b4 * 1e3, 3),
                 "frac_of_hbm_peak": round(WEIGHT_BYTES / (ms_b4 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             },
             "call_us_batch1": round(ms_per_step * 1e3, 3),
-        },
+        }, **sec),
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
@@ -300,6 +358,87 @@ def run_gpu(args):
         print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def _graph_us(torch, fn, calls, reps):
+    ms, _, _ = _graph_time_ms(torch, fn, calls, reps)
+    return ms * 1e3
+
+
+def secondary(torch, gl, peaks):
+    """The other rows of the hot path, each on its own synthetic workload, in
+    CUDA graphs of back-to-back calls over weight copies larger than L2."""
+    import numpy as np
+    from synth import hfp4_gemv, moe_expert_weights, moe_gemv, prefill_gemm
+    out = {}
+    hbm = peaks["hbm_gbs"]
+
+    # MoE bulk-expert GEMV: 256 experts of 768 x 2048, 16 tokens, top-8
+    E, M, K, T, top_k = 256, 768, 2048, 16, 8
+    w = moe_gemv(E=E, M=M, K=K, T=T, top_k=top_k, seed=2, experts=False)
+    copies = 3
+    Pc = torch.empty((copies, E, M, K // 32, 10), dtype=torch.uint8, device="cuda")
+    for e in range(E):
+        gl.rfp2_pack_weights(torch.from_numpy(moe_expert_weights(2, E, M, K, e)).cuda(), out=Pc[0, e])
+    for c in range(1, copies):
+        Pc[c] = Pc[0]
+    ids = torch.from_numpy(w["ids"]).cuda()
+    x = torch.from_numpy(w["x"]).cuda()
+    y = torch.empty((T, top_k, M), dtype=torch.float32, device="cuda")
+    ws = torch.empty(gl.rfp2_moe_workspace_bytes(T, top_k, K), dtype=torch.uint8, device="cuda")
+    touched = len(set(w["ids"].ravel().tolist()))
+    nbytes = touched * M * K // 32 * 10
+    us = _graph_us(torch, lambda i: gl.rfp2_moe_gemv(Pc[i % copies], E, M, K, ids, x, y=y,
+                                                     workspace=ws), 200, 3)
+    out["moe_gemv"] = {
+        "workload": f"256 experts x ROCmFP2 [768, 2048], 16 tokens, top-8 ({touched} experts "
+                    f"touched), seed 2; {copies} copies of all experts rotate",
+        "value": round(nbytes / us / 1e3, 1), "unit": "GB/s (touched experts' packed bytes)",
+        "us_per_call": round(us, 2), "bytes_per_call": nbytes,
+        "frac_of_hbm_peak": round(nbytes / us / 1e3 / hbm, 4)}
+    del Pc, ids, x, y, ws
+
+    # HFP4G32 GEMV 8192 x 8192, batch 1 and 8
+    w = hfp4_gemv(N=8)
+    M, K = w["W"].shape
+    P = gl.hfp4_pack_weights(torch.from_numpy(w["W"]).cuda())
+    copies = 16
+    Pc = torch.empty((copies,) + tuple(P.shape), dtype=torch.uint8, device="cuda")
+    Pc[:] = P
+    for N in (1, 8):
+        x = torch.from_numpy(w["x"][:N].copy()).cuda()
+        y = torch.empty((N, M), dtype=torch.float32, device="cuda")
+        ws = torch.empty(gl.hfp4_gemv_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
+        us = _graph_us(torch, lambda i: gl.hfp4_gemv(Pc[i % copies], M, K, x, y=y, workspace=ws),
+                       200, 3)
+        out[f"hfp4_gemv_batch{N}"] = {
+            "workload": f"HFP4G32 [8192, 8192] N(0, 0.02^2) seed 4, batch {N}; {copies} copies rotate",
+            "value": round(P.numel() / us / 1e3, 1), "unit": "GB/s (packed bytes)",
+            "us_per_call": round(us, 2), "bytes_per_call": int(P.numel()),
+            "frac_of_hbm_peak": round(P.numel() / us / 1e3 / hbm, 4)}
+    del P, Pc
+    torch.cuda.empty_cache()
+
+    # prefill GEMM 17408 x 5120 x 2048 tokens (expansion to bf16 included)
+    w = prefill_gemm()
+    M, K = w["W"].shape
+    N = w["X"].shape[0]
+    P = gl.rfp2_pack_weights(torch.from_numpy(w["W"]).cuda())
+    X = torch.from_numpy(w["X"].view(np.int16)).cuda()
+    Y = torch.empty((N, M), dtype=torch.float32, device="cuda")
+    ws = torch.empty(gl.rfp2_gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    us = _graph_us(torch, lambda i: gl.rfp2_gemm(P, M, K, X, Y=Y, workspace=ws), 20, 3)
+    tflops = 2.0 * M * K * N / us / 1e6
+    out["prefill_gemm"] = {
+        "workload": "ROCmFP2 [17408, 5120] N(0, 0.015^2) x bf16 [2048, 5120] (0.5% x20), seed 3",
+        "value": round(tflops, 1), "unit": "TFLOP/s (2*M*N*K, expansion included)",
+        "us_per_call": round(us, 1),
+        "frac_of_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),
+        "frac_of_bf16_sustained": round(tflops / peaks["bf16_tflops_sustained"], 4),
+        "bound": "tensor", "peak_source": peaks["source"] + " bf16_tflops (cuBLAS bf16)"}
+    del P, X, Y, ws
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(torch, gl, w, Pc, copies, steps):
@@ -327,10 +466,18 @@ def run_e2e(torch, gl, w, Pc, copies, steps):
 # CPU oracle (baseline leg and reference arm)
 
 
+_DECODE_W = None
+
+
 def _oracle_sample(rows: int):
+    """The oracle's own packing of `rows` evenly spaced rows of the decode
+    weights (preparation, untimed) and the batch-1 activations."""
+    global _DECODE_W
     import oracle
     from synth import decode_gemv
-    w = decode_gemv(N=1)
+    if _DECODE_W is None:
+        _DECODE_W = decode_gemv(N=1)
+    w = _DECODE_W
     idx = np.linspace(0, M_DEC - 1, rows).astype(np.int64)
     P = oracle.rfp2_pack(w["W"][idx])
     return oracle, P, w["x"][:1].copy(), idx
@@ -359,7 +506,7 @@ def cpu_baseline(seconds: float, rows: int = 512):
 def run_reference(args):
     """Reference arm: the CPU oracle on the host cores, exactly K steps after W
     warm-up steps; each step is quantize + GEMV over a row sample sized so the
-    whole run stays within about a minute."""
+    whole run stays within --ref-seconds (a minute by default)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -369,8 +516,9 @@ def run_reference(args):
     q, d = orc.quantize_act(x)
     orc.rfp2_gemv(P, 64, K_DEC, q, d)
     per_row = (time.perf_counter() - t0) / 64
-    budget = 60.0 / max(1, args.steps + args.warmup)
-    rows = int(min(M_DEC, max(8, budget / max(per_row, 1e-9))))
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
+    # the oracle packs its sample (about 2 ms a row): keep that preparation short
+    rows = int(min(2048, max(8, budget / max(per_row, 1e-9))))
     orc, P, x, idx = _oracle_sample(rows)
     for _ in range(args.warmup):
         q, d = orc.quantize_act(x)
@@ -405,7 +553,10 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the MoE, HFP4 and prefill GEMM measurements")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="time budget of the reference arm's K + W steps")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per GEMV launch from an ncu capture of this kernel")
     args = ap.parse_args()
