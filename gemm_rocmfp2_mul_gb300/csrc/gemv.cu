@@ -10,9 +10,14 @@
 //    [i*M/G, (i+1)*M/G), so its weights are one contiguous slab.
 //  * A producer warp streams that slab into a ring of shared-memory stages
 //    with 1-D bulk async copies (cp.async.bulk, L2 evict-first), one stage per
-//    chunk of rows, issuing as many stages as fit (~200 KB) before the first
+//    chunk of rows, issuing as many stages as fit (~200 KB, ~100 KB when two
+//    CTAs share the SM) before the first
 //    one is consumed.  Rows of K % 256 == 0 are whole 16-byte units.
-//  * Twelve consumer warps.  Each thread keeps the int8 activations of its
+//  * Batches of at most two quantize x inside the kernel (one launch per
+//    call; every CTA quantizes the whole vector into shared memory) and are
+//    built to run two CTAs per SM: the next call's CTA becomes resident at
+//    once and streams its weights while this call computes.
+//  * Twelve or sixteen consumer warps.  Each thread keeps the int8 activations of its
 //    K-slice for all N columns in registers, reads its BPT blocks of a row
 //    with conflict-free shared loads (strides 20/40/80 B map to distinct
 //    banks) and runs the PRMT + dp4a decode of rfp2_decode.cuh.
@@ -39,16 +44,29 @@ namespace {
 #ifndef RFP2_GEMV_WARPS
 #define RFP2_GEMV_WARPS 12
 #endif
+// The fused-quantize kernel (batch <= 2): consumer warps, CTAs per SM it is
+// compiled for, and its shared-memory budget.  Two CTAs per SM let the next
+// call's CTA start beside the running one and prefetch its weights while this
+// one computes.
+#ifndef RFP2_GEMV_FWARPS
+#define RFP2_GEMV_FWARPS 16
+#endif
+#ifndef RFP2_GEMV_FMINB
+#define RFP2_GEMV_FMINB 2
+#endif
+#ifndef RFP2_GEMV_FUSED_SMEM
+#define RFP2_GEMV_FUSED_SMEM (100 * 1024)
+#endif
 #ifndef RFP2_GEMV_MAX_STAGES
 #define RFP2_GEMV_MAX_STAGES 64
 #endif
-template <int NC>
+template <int NC, bool FQ>
 constexpr int consumer_warps() {
-    return NC == 1 ? RFP2_GEMV_WARPS1 : RFP2_GEMV_WARPS;
+    return FQ ? RFP2_GEMV_FWARPS : NC == 1 ? RFP2_GEMV_WARPS1 : RFP2_GEMV_WARPS;
 }
-template <int NC>
+template <int NC, bool FQ>
 constexpr int gemv_threads() {
-    return (consumer_warps<NC>() + 1) * 32;
+    return (consumer_warps<NC, FQ>() + 1) * 32;
 }
 
 // Rows per warp per chunk: several independent rows per warp amortise the
@@ -61,16 +79,26 @@ constexpr int rows_per_warp() {
     return NC == 1 ? RFP2_GEMV_R1 : NC == 2 ? 2 : 1;
 }
 
-template <int NC, int BPT>
-__global__ void __launch_bounds__(gemv_threads<NC>(), 1)
+// FQ = false: q/d come quantized from global memory (copied to shared memory
+// by the producer warp).  FQ = true: the consumer warps quantize x into shared
+// memory themselves (one launch per call; CTA 0 also writes q/d to global).
+template <int NC, int BPT, bool FQ>
+__global__ void __launch_bounds__(gemv_threads<NC, FQ>(), FQ ? RFP2_GEMV_FMINB : 1)
     gemv_q8_kernel(const uint8_t *__restrict__ W, int M, int K, const int8_t *__restrict__ q,
-                   const float *__restrict__ d, float *__restrict__ y, int32_t *status, int WK,
-                   int stages, int rows_per_cta, int rows_extra) {
+                   const float *__restrict__ d, const float *__restrict__ x, int8_t *qout,
+                   float *dout, float *__restrict__ y, int32_t *status, int WK, int stages,
+                   int rows_per_cta, int rows_extra) {
     extern __shared__ __align__(128) uint8_t smem[];
+#ifndef RFP2_GEMV_NO_EARLY_TRIGGER
+    // fused path: let the next call's grid become resident at once (beside
+    // this CTA) so that its weight stream overlaps this call's compute; its
+    // consumers still wait for this grid to complete before touching x or y
+    if constexpr (FQ) pdl_launch_dependents();
+#endif
     const int KB = K >> 5;
     const int rowbytes = KB * 10;
     constexpr int R = rows_per_warp<NC>();
-    constexpr int CW = consumer_warps<NC>();
+    constexpr int CW = consumer_warps<NC, FQ>();
     const int RG = CW / WK;  // row groups; R rows per group per chunk
     const int CR = RG * R;   // rows per chunk
     Ring r = carve_ring(smem, stages, CR * rowbytes, RG, WK, NextPow2<R * NC>::v);
@@ -92,7 +120,7 @@ __global__ void __launch_bounds__(gemv_threads<NC>(), 1)
     if (producer) {
         // start the weight stream before anything else: the stage barriers
         // are initialised and the first stages issued ahead of the CTA barrier
-        init_ring_stages(r, CW);
+        init_ring_stages(r, CW, FQ ? CW * 32 : 32);
         pol = policy_evict_first();
         for (; c < nchunks && c < stages; ++c) {
             const int rows = min(CR, nrows - c * CR);
@@ -104,9 +132,11 @@ __global__ void __launch_bounds__(gemv_threads<NC>(), 1)
     __syncthreads();
 
     if (warp == CW) {
-        // q and d may come from the kernel launched just before this one
-        pdl_wait();
-        load_act_to_smem(r, lane, act_q, q, qbytes, act_d, d, dbytes);
+        if constexpr (!FQ) {
+            // q and d may come from the kernel launched just before this one
+            pdl_wait();
+            load_act_to_smem(r, lane, act_q, q, qbytes, act_d, d, dbytes);
+        }
         // producer: refill the ring as the consumers release stages
         if (lane == 0) {
             for (; c < nchunks; ++c) {
@@ -125,6 +155,9 @@ __global__ void __launch_bounds__(gemv_threads<NC>(), 1)
     const bool active = kb0 < KB;
     pdl_wait();
     pdl_launch_dependents();
+    if constexpr (FQ)
+        quantize_to_smem(r, warp, CW, lane, x, NC, K, act_q, reinterpret_cast<float *>(act_d),
+                         blockIdx.x == 0 ? qout : nullptr, dout);
     if (!mbar_wait(r.act_bar, 0)) {
         record_status(status, RFP2_ETIMEOUT);
         *r.abort_flag = 1;
@@ -162,14 +195,16 @@ struct Plan {
     size_t smem;
 };
 
-bool make_plan(int NC, int64_t M, int64_t K, Plan &p) {
+bool make_plan(int NC, int64_t M, int64_t K, Plan &p, bool fused = false) {
+    const size_t budget = fused ? (size_t)RFP2_GEMV_FUSED_SMEM : (size_t)kGemvSmemBudget;
     const int KB = (int)(K / 32);
     int bpt = bpt_max(NC);
     while (bpt > 1 && KB < 32 * bpt) bpt /= 2;
     int WK = (KB + 32 * bpt - 1) / (32 * bpt);
     // K-slice warps per row: the smallest divisor of the consumer warp count
     // that covers the row (row groups of CW / WK warps)
-    const int CW = NC == 1 ? consumer_warps<1>() : consumer_warps<2>();
+    const int CW = fused ? consumer_warps<1, true>()
+                   : NC == 1 ? consumer_warps<1, false>() : consumer_warps<2, false>();
     int WKp = 0;
     for (int dv = 1; dv <= CW; ++dv)
         if (CW % dv == 0 && dv >= WK) {
@@ -194,18 +229,18 @@ bool make_plan(int NC, int64_t M, int64_t K, Plan &p) {
     const size_t act = ((size_t)NC * K + 15) / 16 * 16 + (size_t)NC * KB * 4;
     int stages = chunks_per_cta < RFP2_GEMV_MAX_STAGES ? chunks_per_cta : RFP2_GEMV_MAX_STAGES;
     while (stages > 1 &&
-           ring_bytes(stages, p.chunk_bytes, p.RG, p.WK, V) + act > (size_t)kGemvSmemBudget)
+           ring_bytes(stages, p.chunk_bytes, p.RG, p.WK, V) + act > budget)
         --stages;
     p.stages = stages;
     p.smem = ring_bytes(stages, p.chunk_bytes, p.RG, p.WK, V) + act;
     return p.smem <= 227 * 1024;
 }
 
-template <int NC, int BPT>
+template <int NC, int BPT, bool FQ>
 cudaError_t launch_gemv_t(const Plan &p, const uint8_t *W, int M, int K, const int8_t *q,
-                          const float *d, float *y, int32_t *status, cudaStream_t stream,
-                          bool pdl) {
-    auto kern = gemv_q8_kernel<NC, BPT>;
+                          const float *d, const float *x, int8_t *qout, float *dout, float *y,
+                          int32_t *status, cudaStream_t stream, bool pdl) {
+    auto kern = gemv_q8_kernel<NC, BPT, FQ>;
     static std::mutex mu;
     static int configured[64] = {0};
     const int dev = current_device();
@@ -217,49 +252,78 @@ cudaError_t launch_gemv_t(const Plan &p, const uint8_t *W, int M, int K, const i
             configured[dev] = 1;
         }
     }
-    return launch(kern, dim3(p.grid), dim3(gemv_threads<NC>()), p.smem, stream, pdl, W, M, K, q, d, y,
-                  status, p.WK, p.stages, M / p.grid, M % p.grid);
+    return launch(kern, dim3(p.grid), dim3(gemv_threads<NC, FQ>()), p.smem, stream, pdl, W, M, K,
+                  q, d, x, qout, dout, y, status, p.WK, p.stages, M / p.grid, M % p.grid);
 }
 
-template <int NC>
+template <int NC, bool FQ>
 cudaError_t launch_gemv_nc(const Plan &p, const uint8_t *W, int M, int K, const int8_t *q,
-                           const float *d, float *y, int32_t *status, cudaStream_t stream,
-                           bool pdl) {
+                           const float *d, const float *x, int8_t *qout, float *dout, float *y,
+                           int32_t *status, cudaStream_t stream, bool pdl) {
     switch (p.bpt) {
         case 8:
             if constexpr (bpt_max(NC) >= 8)
-                return launch_gemv_t<NC, 8>(p, W, M, K, q, d, y, status, stream, pdl);
+                return launch_gemv_t<NC, 8, FQ>(p, W, M, K, q, d, x, qout, dout, y, status, stream,
+                                                pdl);
             break;
         case 4:
             if constexpr (bpt_max(NC) >= 4)
-                return launch_gemv_t<NC, 4>(p, W, M, K, q, d, y, status, stream, pdl);
+                return launch_gemv_t<NC, 4, FQ>(p, W, M, K, q, d, x, qout, dout, y, status, stream,
+                                                pdl);
             break;
         case 2:
             if constexpr (bpt_max(NC) >= 2)
-                return launch_gemv_t<NC, 2>(p, W, M, K, q, d, y, status, stream, pdl);
+                return launch_gemv_t<NC, 2, FQ>(p, W, M, K, q, d, x, qout, dout, y, status, stream,
+                                                pdl);
             break;
         default:
-            return launch_gemv_t<NC, 1>(p, W, M, K, q, d, y, status, stream, pdl);
+            return launch_gemv_t<NC, 1, FQ>(p, W, M, K, q, d, x, qout, dout, y, status, stream, pdl);
     }
     return cudaErrorInvalidValue;
 }
 
+// GEMV on quantized activations q/d.
 cudaError_t launch_gemv(const uint8_t *W, int64_t M, int64_t K, const int8_t *q, const float *d,
                         int64_t N, float *y, int32_t *status, cudaStream_t stream, bool pdl) {
     Plan p;
     if (!make_plan((int)N, M, K, p)) return cudaErrorInvalidValue;
     const int m = (int)M, k = (int)K;
     switch (N) {
-        case 1: return launch_gemv_nc<1>(p, W, m, k, q, d, y, status, stream, pdl);
-        case 2: return launch_gemv_nc<2>(p, W, m, k, q, d, y, status, stream, pdl);
-        case 3: return launch_gemv_nc<3>(p, W, m, k, q, d, y, status, stream, pdl);
-        case 4: return launch_gemv_nc<4>(p, W, m, k, q, d, y, status, stream, pdl);
-        case 5: return launch_gemv_nc<5>(p, W, m, k, q, d, y, status, stream, pdl);
-        case 6: return launch_gemv_nc<6>(p, W, m, k, q, d, y, status, stream, pdl);
-        case 7: return launch_gemv_nc<7>(p, W, m, k, q, d, y, status, stream, pdl);
-        case 8: return launch_gemv_nc<8>(p, W, m, k, q, d, y, status, stream, pdl);
+#define RFP2_CASE(n)                                                                            \
+    case n:                                                                                     \
+        return launch_gemv_nc<n, false>(p, W, m, k, q, d, nullptr, nullptr, nullptr, y, status, \
+                                        stream, pdl);
+        RFP2_CASE(1)
+        RFP2_CASE(2)
+        RFP2_CASE(3)
+        RFP2_CASE(4)
+        RFP2_CASE(5)
+        RFP2_CASE(6)
+        RFP2_CASE(7)
+        RFP2_CASE(8)
+#undef RFP2_CASE
     }
     return cudaErrorInvalidValue;
+}
+
+// Batches of at most 2 whose activations fit beside a weight ring: quantize
+// inside the GEMV (one launch per call); q and d also go to qout/dout.
+bool fused_applies(int64_t M, int64_t K, int64_t N) {
+    Plan p;
+    return N <= 2 && make_plan((int)N, M, K, p, true);
+}
+
+cudaError_t launch_gemv_fused(const uint8_t *W, int64_t M, int64_t K, const float *x, int64_t N,
+                              int8_t *qout, float *dout, float *y, int32_t *status,
+                              cudaStream_t stream) {
+    Plan p;
+    if (!make_plan((int)N, M, K, p, true)) return cudaErrorInvalidValue;
+    const int m = (int)M, k = (int)K;
+    if (N == 1)
+        return launch_gemv_nc<1, true>(p, W, m, k, nullptr, nullptr, x, qout, dout, y, status,
+                                       stream, true);
+    return launch_gemv_nc<2, true>(p, W, m, k, nullptr, nullptr, x, qout, dout, y, status, stream,
+                                   true);
 }
 
 rfp2_status check_gemv_shape(int64_t M, int64_t K, int64_t N) {
@@ -311,6 +375,8 @@ extern "C" rfp2_status rfp2_gemv(const uint8_t *W, int64_t M, int64_t K, const f
     int8_t *q = static_cast<int8_t *>(workspace);
     float *d = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
                                          ((size_t)(N * K) + 255) / 256 * 256);
+    if (fused_applies(M, K, N))
+        return from_cuda(launch_gemv_fused(W, M, K, x, N, q, d, y, dev_status, s));
     cudaError_t e = launch_quantize(x, N, K, q, d, s, true);
     if (e != cudaSuccess) return RFP2_ECUDA;
     return from_cuda(launch_gemv(W, M, K, q, d, N, y, dev_status, s, true));

@@ -216,12 +216,12 @@ __host__ __device__ inline size_t ring_bytes(int nstages, int chunk_bytes, int R
 // Initialise the ring's stage barriers (one thread, the producer) and make
 // them visible to the async proxy; the caller may issue bulk copies on them
 // right away, before the CTA-wide barrier.
-RFP2_DEV void init_ring_stages(Ring &r, int consumer_warps) {
+RFP2_DEV void init_ring_stages(Ring &r, int consumer_warps, int act_arrivals = 32) {
     for (int s = 0; s < r.nstages; ++s) {
         mbar_init(&r.full[s], 1);
         mbar_init(&r.empty[s], consumer_warps);
     }
-    mbar_init(r.act_bar, 32);
+    mbar_init(r.act_bar, act_arrivals);
     *r.abort_flag = 0;
     fence_mbar_init();
 }
@@ -280,6 +280,99 @@ RFP2_DEV void load_act_to_smem(Ring &r, int lane, uint8_t *dst_q, const int8_t *
             if (i < n) {
                 if (i < nq) tq[act_swizzle(i)] = v[j];
                 else td[i - nq] = v[j];
+            }
+        }
+    }
+    mbar_arrive(r.act_bar);
+}
+
+RFP2_DEV float rcp_approx(float v) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// Consumer warps (warp index w of cw): quantize x fp32 [nc, K] into the
+// staged, swizzled activation layout, then arrive (every lane) on the
+// activation barrier; with `gq`/`gd` set, q and d also go to global memory.
+// Same results as the quantize kernel (Q8_1-style blocks: d = amax / 127 and
+// q = roundf(a / d) with IEEE division), computed with less latency:
+//  * QB blocks per warp are in flight together (loads, max-reductions);
+//  * each d is divided once, by the lane whose index is the block's slot,
+//    and broadcast;
+//  * q comes from z = a * rcp.approx(d), whose relative error is below
+//    2^-22.  The IEEE quotient fl(a/d) lies within 2^-24 of a/d, so both
+//    round to the same integer unless a/d is within about 2^-21 |z| of a
+//    half-integer; lanes whose z is within 2^-19 |z| of one (or is not
+//    finite) take the IEEE division and roundf instead.
+#ifndef RFP2_GEMV_QB
+#define RFP2_GEMV_QB 8
+#endif
+RFP2_DEV void quantize_to_smem(Ring &r, int w, int cw, int lane, const float *__restrict__ x,
+                               int nc, int K, uint8_t *act_q, float *act_d, int8_t *gq,
+                               float *gd) {
+    const int nblk = nc * (K >> 5);
+    constexpr int QB = RFP2_GEMV_QB;
+    // every CTA reads all of x at the same moment: start each CTA at a
+    // different block so the requests spread over the L2 slices
+    const int rot = (int)((blockIdx.x * 8u) % (unsigned)nblk);
+    for (int b0 = w; b0 < nblk; b0 += cw * QB) {
+        float a[QB], m[QB];
+        int bb[QB];
+#pragma unroll
+        for (int j = 0; j < QB; ++j) {
+            const int b = b0 + j * cw;
+            bb[j] = b + rot < nblk ? b + rot : b + rot - nblk;
+            a[j] = b < nblk ? __ldg(x + (int64_t)bb[j] * 32 + lane) : 0.0f;
+            m[j] = fabsf(a[j]);
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+            for (int j = 0; j < QB; ++j) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], off));
+        // lane j divides for block slot j; d and 1/d are broadcast
+        float mine = m[0];
+#pragma unroll
+        for (int j = 1; j < QB; ++j)
+            if (lane == j) mine = m[j];
+        const float dmine = __fdiv_rn(mine, 127.0f);
+        const float rmine = rcp_approx(dmine);
+        // branch-free over the QB blocks so that their latencies overlap;
+        // z + 1.5*2^23 rounds z to the nearest integer (|z| < 2^22) and holds
+        // it in its low mantissa bits; away from half-integers that equals
+        // roundf(z)
+        float dd[QB];
+        int qv[QB];
+        uint32_t need = 0;
+#pragma unroll
+        for (int j = 0; j < QB; ++j) {
+            dd[j] = __shfl_sync(0xffffffffu, dmine, j);
+            const float z = a[j] * __shfl_sync(0xffffffffu, rmine, j);
+            const float zb = z + 12582912.0f;
+            const float e = fabsf(z - (zb - 12582912.0f));
+            const bool exact =
+                dd[j] != 0.0f && !(0.5f - e > fmaf(fabsf(z), 0x1p-19f, 0x1p-30f));
+            need |= (uint32_t)exact << j;
+            const int qi = min(max(__float_as_int(zb) - 0x4B400000, -127), 127);
+            qv[j] = dd[j] != 0.0f ? qi : 0;
+        }
+        if (__any_sync(0xffffffffu, need != 0)) {
+#pragma unroll
+            for (int j = 0; j < QB; ++j)
+                if ((need >> j) & 1u)
+                    qv[j] = static_cast<int>(
+                        fminf(fmaxf(roundf(__fdiv_rn(a[j], dd[j])), -127.0f), 127.0f));
+        }
+#pragma unroll
+        for (int j = 0; j < QB; ++j) {
+            if (b0 + j * cw < nblk) {  // warp-uniform
+                const uint32_t i = (uint32_t)bb[j] * 32 + lane;
+                act_q[act_swizzle(i >> 4) * 16 + (i & 15)] = (uint8_t)qv[j];
+                if (lane == 0) act_d[bb[j]] = dd[j];
+                if (gq) {
+                    gq[i] = (int8_t)qv[j];
+                    if (lane == 0) gd[bb[j]] = dd[j];
+                }
             }
         }
     }

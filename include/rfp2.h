@@ -107,9 +107,15 @@ rfp2_status rfp2_gemv_q8(const uint8_t *W, int64_t M, int64_t K, const int8_t *q
 size_t rfp2_gemv_workspace_bytes(int64_t N, int64_t K);
 
 /* ---------------------------------------------------------------------------
- * ROCmFP2 GEMV from fp32 activations: quantizes x into `workspace` (q then
- * d) and runs the GEMV, as two launches chained with programmatic dependent
- * launch so the weight stream starts while x is quantized.
+ * ROCmFP2 GEMV from fp32 activations: quantizes x (q then d, written to
+ * `workspace`) and runs the GEMV.  For N <= 2 (when the activations fit in
+ * shared memory beside a weight ring) the quantization runs inside the GEMV
+ * kernel, one launch per call; otherwise it is a separate kernel chained to
+ * the GEMV with programmatic dependent launch.  Either way the GEMV starts
+ * streaming W before the kernel enqueued just before it on the stream has
+ * finished (x, the workspace and y are touched only after it has), so W must
+ * not be written by that preceding kernel: after writing W, synchronize the
+ * stream before the first call.
  *   x fp32 [N, K] device; y fp32 [N, M] device; workspace device, at least
  *   rfp2_gemv_workspace_bytes(N, K) bytes, 256-byte aligned; after the call
  *   it holds q int8 [N, K] followed (at offset rounded up to 256) by d.

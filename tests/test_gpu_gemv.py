@@ -48,6 +48,19 @@ def _inputs(kind, N, K, seed=0):
         x = rng.standard_t(3, (N, K)) * 1e-3
     elif kind == "wide":
         x = rng.normal(0, 1, (N, K)) * 10.0 ** rng.integers(-6, 6, (N, K // 32, 1)).repeat(32, 2).reshape(N, K)
+    elif kind == "ties":
+        # a / d within a few ulps of a half-integer, for scales d that are
+        # not powers of two: the rounding decision sits at its boundary
+        d = (rng.random((N, K // 32, 1)) + 0.5).astype(np.float32)
+        k = rng.integers(-127, 127, (N, K // 32, 32)).astype(np.float32) + 0.5
+        x = (k * d).astype(np.float32)
+        ulps = rng.integers(-3, 4, x.shape)
+        x = np.nextafter(x, np.where(ulps > 0, np.inf, -np.inf).astype(np.float32)) * (ulps != 0) + x * (ulps == 0)
+        x[:, :, 0] = 127.0 * d[:, :, 0]
+        x = x.reshape(N, K)
+    elif kind == "subnormal":
+        # block maxima near and below the smallest normal: d is subnormal
+        x = rng.normal(0, 1, (N, K)) * 10.0 ** rng.integers(-44, -36, (N, K // 32, 1)).repeat(32, 2).reshape(N, K)
     else:
         x = rng.normal(0, 1, (N, K))
         x[:, :64] = 0.0
@@ -60,7 +73,10 @@ def _inputs(kind, N, K, seed=0):
 
 # -- activation quantization ------------------------------------------------------
 
-@pytest.mark.parametrize("kind", ["normal", "student_t", "wide", "edge"])
+KINDS = ["normal", "student_t", "wide", "edge", "ties", "subnormal"]
+
+
+@pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("N,K", [(1, 4096), (4, 2048), (8, 256), (3, 8192)])
 def test_quantize_bit_exact(g, kind, N, K):
     x = _inputs(kind, N, K, seed=N * K)
@@ -68,6 +84,29 @@ def test_quantize_bit_exact(g, kind, N, K):
     qo, do = oracle.quantize_act(x)
     np.testing.assert_array_equal(host(d), do)
     np.testing.assert_array_equal(host(q), qo)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("N,K", [(1, 4096), (2, 2048), (1, 256), (2, 16384)])
+def test_gemv_quantize_bit_exact(g, kind, N, K):
+    """rfp2_gemv quantizes inside the GEMV kernel at batch <= 2; the q and d it
+    leaves in the workspace are the oracle's, bit for bit."""
+    import torch
+    x = _inputs(kind, N, K, seed=7 * N + K)
+    W = normal_weights(np.random.default_rng(K), 160, K, 0.02)
+    P = oracle.rfp2_pack(W)
+    ws = torch.zeros(g.rfp2_gemv_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
+    st = status_tensor()
+    y = host(g.rfp2_gemv(dev(P), 160, K, dev(x), workspace=ws, dev_status=st))
+    assert host(st)[0] == 0
+    qo, do = oracle.quantize_act(x)
+    wsh = host(ws)
+    np.testing.assert_array_equal(wsh[:N * K].view(np.int8).reshape(N, K), qo)
+    off = (N * K + 255) // 256 * 256
+    np.testing.assert_array_equal(wsh[off:off + N * K // 32 * 4].view(np.float32).reshape(N, -1), do)
+    ref = oracle.rfp2_gemv(P, 160, K, qo, do)
+    if np.all(np.abs(ref).max(axis=1) > 0):
+        assert np.all(rel_err_rows(y, ref) <= TOL)
 
 
 # -- packers ------------------------------------------------------------------------
@@ -164,7 +203,7 @@ def _gemv_case(g, M, K, N, seed, fused=True):
 @pytest.mark.parametrize("M,K,N", [
     (256, 1024, 1), (1000, 4096, 1), (1000, 4096, 4), (777, 2048, 3), (64, 256, 8),
     (333, 8192, 2), (50, 5120, 4), (130, 768, 5), (300, 1536, 6), (129, 2048, 7),
-    (1, 4096, 8), (5, 256, 1), (2048, 4096, 2),
+    (1, 4096, 8), (5, 256, 1), (2048, 4096, 2), (64, 16384, 1), (40, 32768, 2),
 ])
 def test_gemv_parity(g, M, K, N):
     y, ref = _gemv_case(g, M, K, N, seed=M + K + N)
