@@ -36,7 +36,10 @@ struct Log2<1> {
 
 // Largest blocks-per-thread for NC columns: keeps 8*BPT*NC activation words
 // (<= 64 registers) resident.
-constexpr int bpt_max(int nc) { return nc <= 2 ? 4 : nc <= 4 ? 2 : 1; }
+#ifndef RFP2_GEMV_BPT12
+#define RFP2_GEMV_BPT12 4
+#endif
+constexpr int bpt_max(int nc) { return nc <= 2 ? RFP2_GEMV_BPT12 : nc <= 4 ? 2 : 1; }
 
 // Activations of one thread: [column][block][half][word] permuted int8 words
 // and the per-block scale dA.
@@ -296,83 +299,100 @@ RFP2_DEV float rcp_approx(float v) {
 // staged, swizzled activation layout, then arrive (every lane) on the
 // activation barrier; with `gq`/`gd` set, q and d also go to global memory.
 // Same results as the quantize kernel (Q8_1-style blocks: d = amax / 127 and
-// q = roundf(a / d) with IEEE division), computed with less latency:
-//  * QB blocks per warp are in flight together (loads, max-reductions);
-//  * each d is divided once, by the lane whose index is the block's slot,
-//    and broadcast;
+// q = roundf(a / d) with IEEE division), computed with few instructions:
+//  * eight lanes per 32-value block, four values per lane, so a warp covers
+//    four blocks per step and QB steps are in flight together;
 //  * q comes from z = a * rcp.approx(d), whose relative error is below
 //    2^-22.  The IEEE quotient fl(a/d) lies within 2^-24 of a/d, so both
 //    round to the same integer unless a/d is within about 2^-21 |z| of a
 //    half-integer; lanes whose z is within 2^-19 |z| of one (or is not
-//    finite) take the IEEE division and roundf instead.
+//    finite) take the IEEE division and roundf instead.  Away from
+//    half-integers z + 1.5*2^23 rounds z to that integer and holds it in its
+//    low mantissa bits; |z| <= 127 (1 + 2^-22) needs no clamp.
 #ifndef RFP2_GEMV_QB
-#define RFP2_GEMV_QB 8
+#define RFP2_GEMV_QB 2
 #endif
 RFP2_DEV void quantize_to_smem(Ring &r, int w, int cw, int lane, const float *__restrict__ x,
                                int nc, int K, uint8_t *act_q, float *act_d, int8_t *gq,
                                float *gd) {
     const int nblk = nc * (K >> 5);
     constexpr int QB = RFP2_GEMV_QB;
+    const int sub = lane >> 3, l8 = lane & 7;
+    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
     // every CTA reads all of x at the same moment: start each CTA at a
     // different block so the requests spread over the L2 slices
     const int rot = (int)((blockIdx.x * 8u) % (unsigned)nblk);
-    for (int b0 = w; b0 < nblk; b0 += cw * QB) {
-        float a[QB], m[QB];
+    for (int s0 = w * 4; s0 < nblk; s0 += cw * 4 * QB) {
+        float v[QB][4];
         int bb[QB];
+        bool ok[QB];
 #pragma unroll
         for (int j = 0; j < QB; ++j) {
-            const int b = b0 + j * cw;
+            const int b = s0 + j * cw * 4 + sub;
+            ok[j] = b < nblk;
             bb[j] = b + rot < nblk ? b + rot : b + rot - nblk;
-            a[j] = b < nblk ? __ldg(x + (int64_t)bb[j] * 32 + lane) : 0.0f;
-            m[j] = fabsf(a[j]);
-        }
+            const float *src = x + (int64_t)bb[j] * 32 + l8 * 4;
+            if (!ok[j]) {
+                v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0.0f;
+            } else if (vec) {
+                const float4 t = __ldg(reinterpret_cast<const float4 *>(src));
+                v[j][0] = t.x;
+                v[j][1] = t.y;
+                v[j][2] = t.z;
+                v[j][3] = t.w;
+            } else {
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
+                for (int e = 0; e < 4; ++e) v[j][e] = __ldg(src + e);
+            }
+        }
+        float m[QB];
+#pragma unroll
+        for (int j = 0; j < QB; ++j)
+            m[j] = fmaxf(fmaxf(fabsf(v[j][0]), fabsf(v[j][1])), fmaxf(fabsf(v[j][2]), fabsf(v[j][3])));
+#pragma unroll
+        for (int off = 4; off >= 1; off >>= 1)
 #pragma unroll
             for (int j = 0; j < QB; ++j) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], off));
-        // lane j divides for block slot j; d and 1/d are broadcast
-        float mine = m[0];
-#pragma unroll
-        for (int j = 1; j < QB; ++j)
-            if (lane == j) mine = m[j];
-        const float dmine = __fdiv_rn(mine, 127.0f);
-        const float rmine = rcp_approx(dmine);
-        // branch-free over the QB blocks so that their latencies overlap;
-        // z + 1.5*2^23 rounds z to the nearest integer (|z| < 2^22) and holds
-        // it in its low mantissa bits; away from half-integers that equals
-        // roundf(z)
-        float dd[QB];
-        int qv[QB];
-        uint32_t need = 0;
+        float dd[QB], rc[QB];
+        uint32_t word[QB];
+        bool need = false;
 #pragma unroll
         for (int j = 0; j < QB; ++j) {
-            dd[j] = __shfl_sync(0xffffffffu, dmine, j);
-            const float z = a[j] * __shfl_sync(0xffffffffu, rmine, j);
-            const float zb = z + 12582912.0f;
-            const float e = fabsf(z - (zb - 12582912.0f));
-            const bool exact =
-                dd[j] != 0.0f && !(0.5f - e > fmaf(fabsf(z), 0x1p-19f, 0x1p-30f));
-            need |= (uint32_t)exact << j;
-            const int qi = min(max(__float_as_int(zb) - 0x4B400000, -127), 127);
-            qv[j] = dd[j] != 0.0f ? qi : 0;
-        }
-        if (__any_sync(0xffffffffu, need != 0)) {
+            dd[j] = __fdiv_rn(m[j], 127.0f);
+            rc[j] = dd[j] != 0.0f ? rcp_approx(dd[j]) : 0.0f;
+            uint32_t wq = 0;
 #pragma unroll
-            for (int j = 0; j < QB; ++j)
-                if ((need >> j) & 1u)
-                    qv[j] = static_cast<int>(
-                        fminf(fmaxf(roundf(__fdiv_rn(a[j], dd[j])), -127.0f), 127.0f));
+            for (int e = 0; e < 4; ++e) {
+                const float z = v[j][e] * rc[j];
+                const float zb = z + 12582912.0f;
+                const float dist = fabsf(z - (zb - 12582912.0f));
+                need |= !(fmaf(fabsf(z), 0x1p-19f, dist) < 0.5f - 0x1p-30f);
+                wq |= ((uint32_t)(__float_as_int(zb) - 0x4B400000) & 0xFFu) << (8 * e);
+            }
+            word[j] = wq;
         }
+        if (__any_sync(0xffffffffu, need) && need) {
 #pragma unroll
-        for (int j = 0; j < QB; ++j) {
-            if (b0 + j * cw < nblk) {  // warp-uniform
-                const uint32_t i = (uint32_t)bb[j] * 32 + lane;
-                act_q[act_swizzle(i >> 4) * 16 + (i & 15)] = (uint8_t)qv[j];
-                if (lane == 0) act_d[bb[j]] = dd[j];
-                if (gq) {
-                    gq[i] = (int8_t)qv[j];
-                    if (lane == 0) gd[bb[j]] = dd[j];
+            for (int j = 0; j < QB; ++j) {
+                if (dd[j] == 0.0f) continue;
+                uint32_t wq = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float qf = fminf(fmaxf(roundf(__fdiv_rn(v[j][e], dd[j])), -127.0f), 127.0f);
+                    wq |= ((uint32_t)static_cast<int>(qf) & 0xFFu) << (8 * e);
                 }
+                word[j] = wq;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < QB; ++j) {
+            if (!ok[j]) continue;
+            const uint32_t i = (uint32_t)bb[j] * 32 + l8 * 4;
+            *reinterpret_cast<uint32_t *>(act_q + act_swizzle(i >> 4) * 16 + (i & 15)) = word[j];
+            if (l8 == 0) act_d[bb[j]] = dd[j];
+            if (gq) {
+                *reinterpret_cast<uint32_t *>(gq + i) = word[j];
+                if (l8 == 0) gd[bb[j]] = dd[j];
             }
         }
     }
@@ -411,17 +431,20 @@ RFP2_DEV bool consume_chunk(Ring &r, int c, int wg, int wk, int lane, int kb0, b
     float vals[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) vals[i] = 0.0f;
-    const uint8_t *base = r.stages + (size_t)s * r.chunk_bytes + (size_t)wg * R * rowbytes + kb0 * 10;
+    // Straight-line over the R rows so their decodes interleave: a row past
+    // the end of the slab still lies inside the stage and is computed but
+    // never stored; an inactive lane (beyond K) reads the row start and has
+    // zero activations.
+    const uint8_t *base = r.stages + (size_t)s * r.chunk_bytes + (size_t)wg * R * rowbytes +
+                          (active ? kb0 * 10 : 0);
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) {
-        if (valid[rr] && active) {
-            float o[NC];
+        float o[NC];
 #pragma unroll
-            for (int n = 0; n < NC; ++n) o[n] = 0.0f;
-            row_dot<NC, BPT>(base + rr * rowbytes, A, o);
+        for (int n = 0; n < NC; ++n) o[n] = 0.0f;
+        row_dot<NC, BPT>(base + rr * rowbytes, A, o);
 #pragma unroll
-            for (int n = 0; n < NC; ++n) vals[rr * NC + n] = o[n];
-        }
+        for (int n = 0; n < NC; ++n) vals[rr * NC + n] = o[n];
     }
     float total = warp_transpose_reduce<V>(vals, lane);
     const int idx = lane >> (5 - L);
