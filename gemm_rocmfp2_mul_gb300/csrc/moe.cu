@@ -7,15 +7,18 @@
 // Three launches chained with programmatic dependent launch:
 //  1. route (one CTA): validates the ids (an id outside [0, E) is never
 //     dereferenced: its output row is filled with NaN and RFP2_EBADID is
-//     recorded), sorts the (token, slot) pairs by expert and cuts each
-//     expert's run into groups of at most 4 pairs.  Groups go to the
-//     workspace.
+//     recorded), ranks the (token, slot) pairs by expert (several threads per
+//     pair) and cuts each expert's run into groups of at most two pairs
+//     (two tokens' activations fit in registers beside four rows per warp).
+//     Groups go to the workspace.
 //  2. quantize the T tokens once (Q8_1-style blocks) into the workspace.
 //  3. moe_gemv (persistent, one CTA per SM): work units are (group, tile of
 //     rows of that expert); CTA i takes a contiguous range of units, its
 //     producer warp streams the expert rows into the shared-memory ring and
 //     the consumer warps expand every block once for the group's tokens.
-//     Expert offsets are 64-bit.
+//     The group list, the pair order and the quantized tokens are first
+//     copied into shared memory by all threads together (one memory round
+//     trip).  Expert offsets are 64-bit.
 #include <mutex>
 
 #include "common.cuh"
@@ -25,11 +28,24 @@
 namespace rfp2 {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+#ifndef RFP2_MOE_WARPS
+#define RFP2_MOE_WARPS 16
+#endif
+#ifndef RFP2_MOE_COLS
+#define RFP2_MOE_COLS 2
+#endif
+#ifndef RFP2_MOE_ROWS
+#define RFP2_MOE_ROWS 4
+#endif
+#ifndef RFP2_MOE_CHUNKS_PER_TILE
+#define RFP2_MOE_CHUNKS_PER_TILE 1
+#endif
+constexpr int kConsumerWarps = RFP2_MOE_WARPS;
 constexpr int kGemvThreads = (kConsumerWarps + 1) * 32;
-constexpr int kGroupCols = 4;        // tokens per group (activation registers)
-constexpr int kBpt = 2;              // bpt_max(4)
-constexpr int kChunksPerTile = 8;    // rows per unit = 8 chunks of RG rows
+constexpr int kGroupCols = RFP2_MOE_COLS;  // tokens per group (activation registers)
+constexpr int kBpt = 2;                    // blocks per thread
+constexpr int kRows = RFP2_MOE_ROWS;       // rows per warp per chunk
+constexpr int kChunksPerTile = RFP2_MOE_CHUNKS_PER_TILE;  // rows per unit = chunks of RG*kRows
 constexpr int kMaxPairs = 4096;
 constexpr int kRouteThreads = 1024;
 
@@ -105,59 +121,78 @@ __device__ void block_exclusive_scan(int *v, int n, int *warp_sums) {
     __syncthreads();
 }
 
+// Shared memory of the routing pass: sid, gidx and erank (ints), left
+// (shorts) and flag (bytes), P entries each.
+size_t route_smem_bytes(int P) { return (size_t)P * (4 + 4 + 4 + 2 + 1) + 16; }
+
 __global__ void __launch_bounds__(kRouteThreads, 1)
     moe_route_kernel(const int32_t *__restrict__ ids, int P, int64_t E, int M, float *y,
                      int32_t *status, MoeWs w) {
-    __shared__ int sid[kMaxPairs];         // expert of pair p, -1 if invalid
-    __shared__ int gidx[kMaxPairs];        // by sorted position: group-start flag, then index
-    __shared__ short left[kMaxPairs];      // by sorted position: pairs left in the expert run
-    __shared__ unsigned char flag[kMaxPairs];
+    extern __shared__ __align__(16) int rsm[];
+    int *sid = rsm;              // expert of pair p, -1 if invalid
+    int *gidx = sid + P;         // by sorted position: group-start flag, then group index
+    int *erank = gidx + P;       // by sorted position: expert
+    short *left = reinterpret_cast<short *>(erank + P);  // pairs left in the expert run
+    unsigned char *flag = reinterpret_cast<unsigned char *>(left + P);
     __shared__ int warp_sums[32];
-    __shared__ int nvalid_s;
     pdl_wait();
     pdl_launch_dependents();
     const int tid = threadIdx.x;
-    if (tid == 0) nvalid_s = 0;
-    __syncthreads();
-    for (int p = tid; p < P; p += blockDim.x) {
-        const int32_t e = ids[p];
-        const bool ok = e >= 0 && (int64_t)e < E;
-        sid[p] = ok ? e : -1;
-        if (!ok) record_status(status, RFP2_EBADID);
-        else atomicAdd(&nvalid_s, 1);
-    }
-    __syncthreads();
-    const int nvalid = nvalid_s;
-    // NaN rows for invalid pairs (their ids are never used as expert offsets)
-    for (int p = 0; p < P; ++p) {
-        if (sid[p] >= 0) continue;
-        for (int m = tid; m < M; m += blockDim.x) y[(int64_t)p * M + m] = __int_as_float(0x7fc00000);
-    }
-    // rank of each valid pair by (expert, p), its position inside the
-    // expert's run and the run length
-    for (int p = tid; p < P; p += blockDim.x) {
-        const int e = sid[p];
-        if (e < 0) continue;
-        int rank = 0, before = 0, count = 0;
-        for (int p2 = 0; p2 < P; ++p2) {
-            const int e2 = sid[p2];
-            if (e2 < 0) continue;
-            rank += (e2 < e) || (e2 == e && p2 < p);
-            before += e2 < e;
-            count += e2 == e;
+    int nvalid = 0;
+    for (int base = 0; base < P; base += blockDim.x) {
+        const int p = base + tid;
+        bool ok = false;
+        if (p < P) {
+            const int32_t e = ids[p];
+            ok = e >= 0 && (int64_t)e < E;
+            sid[p] = ok ? e : -1;
+            if (!ok) record_status(status, RFP2_EBADID);
         }
-        const int pos = rank - before;
-        w.sorted[rank] = p;
-        flag[rank] = (pos % kGroupCols) == 0;
-        gidx[rank] = (pos % kGroupCols) == 0;
-        left[rank] = (short)(count - pos);
+        nvalid += __syncthreads_count(ok);
+    }
+    // NaN rows for invalid pairs (their ids are never used as expert offsets)
+    if (nvalid < P) {
+        for (int64_t i = tid; i < (int64_t)P * M; i += blockDim.x)
+            if (sid[i / M] < 0) y[i] = __int_as_float(0x7fc00000);
+    }
+    // Rank of each valid pair by (expert, p), its position inside the expert's
+    // run and the run length: tpp threads per pair each scan every tpp-th pair,
+    // then sum over their aligned lane group.
+    int tpp = 1;
+    while (tpp < 32 && tpp * P < (int)blockDim.x) tpp *= 2;
+    const int ppr = blockDim.x / tpp, j = tid & (tpp - 1);
+    for (int p0 = 0; p0 < P; p0 += ppr) {
+        const int p = p0 + tid / tpp;
+        const int e = p < P ? sid[p] : -1;
+        int rank = 0, before = 0, count = 0;
+        if (e >= 0) {
+            for (int p2 = j; p2 < P; p2 += tpp) {
+                const int e2 = sid[p2];
+                if (e2 < 0) continue;
+                rank += (e2 < e) || (e2 == e && p2 < p);
+                before += e2 < e;
+                count += e2 == e;
+            }
+        }
+        for (int off = 1; off < tpp; off <<= 1) {
+            rank += __shfl_xor_sync(0xffffffffu, rank, off);
+            before += __shfl_xor_sync(0xffffffffu, before, off);
+            count += __shfl_xor_sync(0xffffffffu, count, off);
+        }
+        if (e >= 0 && j == 0) {
+            const int pos = rank - before;
+            w.sorted[rank] = p;
+            erank[rank] = e;
+            flag[rank] = (pos % kGroupCols) == 0;
+            gidx[rank] = (pos % kGroupCols) == 0;
+            left[rank] = (short)(count - pos);
+        }
     }
     __syncthreads();
     block_exclusive_scan(gidx, nvalid, warp_sums);  // gidx[r] = starts before r
     for (int r = tid; r < nvalid; r += blockDim.x) {
         if (!flag[r]) continue;
-        const int e = sid[w.sorted[r]];
-        w.groups[gidx[r]] = make_int4(e, r, min(kGroupCols, (int)left[r]), 0);
+        w.groups[gidx[r]] = make_int4(erank[r], r, min(kGroupCols, (int)left[r]), 0);
     }
     if (tid == 0) {
         w.header[0] = nvalid > 0 ? gidx[nvalid - 1] + flag[nvalid - 1] : 0;
@@ -169,7 +204,8 @@ struct MoeArgs {
     const uint8_t *W;
     int64_t expert_bytes;
     int M, K, T, top_k, WK, nstages, tile_rows;
-    int act_staged;  // token activations staged in shared memory
+    int act_staged;   // token activations staged in shared memory
+    int meta_staged;  // group list and pair order staged in shared memory
     float *y;
     int32_t *status;
     MoeWs ws;
@@ -178,12 +214,12 @@ struct MoeArgs {
 template <int NC>
 __device__ bool consume_group(Ring &r, const MoeArgs &a, int4 grp, int t_begin, int t_end, int &c,
                               int wg, int wk, int lane, int kb0, bool active, int rowbytes,
-                              const int8_t *q, const float *d, bool staged) {
+                              const int8_t *q, const float *d, bool staged, const int *sorted) {
     int cols[NC];
     float *ycol[NC];
 #pragma unroll
     for (int n = 0; n < NC; ++n) {
-        const int pair = a.ws.sorted[grp.y + n];
+        const int pair = sorted[grp.y + n];
         cols[n] = pair / a.top_k;
         ycol[n] = a.y + (int64_t)pair * a.M;
     }
@@ -195,16 +231,68 @@ __device__ bool consume_group(Ring &r, const MoeArgs &a, int4 grp, int t_begin, 
     for (int t = t_begin; t < t_end; ++t) {
         const int r0 = t * a.tile_rows;
         const int r1 = min(a.M, r0 + a.tile_rows);
-        const int nch = (r1 - r0 + r.RG - 1) / r.RG;
+        const int cr = r.RG * kRows;
+        const int nch = (r1 - r0 + cr - 1) / cr;
         for (int ch = 0; ch < nch; ++ch, ++c) {
-            const int64_t rows[1] = {r0 + (int64_t)ch * r.RG + wg};
-            const bool valid[1] = {rows[0] < r1};
-            if (!consume_chunk<NC, kBpt, 1>(r, c, wg, wk, lane, kb0, active, rowbytes, rows, valid,
-                                            A, ycol, a.status))
+            int64_t rows[kRows];
+            bool valid[kRows];
+#pragma unroll
+            for (int rr = 0; rr < kRows; ++rr) {
+                rows[rr] = r0 + (int64_t)ch * cr + wg * kRows + rr;
+                valid[rr] = rows[rr] < r1;
+            }
+            if (!consume_chunk<NC, kBpt, kRows>(r, c, wg, wk, lane, kb0, active, rowbytes, rows,
+                                                valid, A, ycol, a.status))
                 return false;
         }
     }
     return true;
+}
+
+// Cooperative copy, global -> shared, of the token activations (q swizzled,
+// then d) and of the group list and pair order: every thread keeps up to
+// eight 16-byte loads in flight, so the whole copy costs about one memory
+// round trip.
+__device__ void stage_inputs(const MoeArgs &a, int ngroups, int nvalid, uint8_t *act_q,
+                             uint8_t *act_d, int4 *sgroups, int *ssorted) {
+    const uint32_t nq = a.act_staged ? (uint32_t)a.T * a.K / 16 : 0;
+    const uint32_t nd = a.act_staged ? (uint32_t)a.T * (a.K / 32) * 4 / 16 : 0;
+    const uint32_t ng = a.meta_staged ? (uint32_t)ngroups : 0;
+    const uint32_t ns = a.meta_staged ? (uint32_t)(nvalid + 3) / 4 : 0;
+    const uint32_t n = nq + nd + ng + ns;
+    const uint4 *srcq = reinterpret_cast<const uint4 *>(a.ws.q);
+    const uint4 *srcd = reinterpret_cast<const uint4 *>(a.ws.d);
+    const uint4 *srcg = reinterpret_cast<const uint4 *>(a.ws.groups);
+    const uint4 *srcs = reinterpret_cast<const uint4 *>(a.ws.sorted);
+    uint4 *dq = reinterpret_cast<uint4 *>(act_q);
+    uint4 *dd = reinterpret_cast<uint4 *>(act_d);
+    uint4 *dg = reinterpret_cast<uint4 *>(sgroups);
+    uint4 *ds = reinterpret_cast<uint4 *>(ssorted);
+    for (uint32_t base = 0; base < n; base += 8 * blockDim.x) {
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t i = base + j * blockDim.x + threadIdx.x;
+            if (i >= n) continue;
+            if (i < nq) { v[j] = srcq[i]; continue; }
+            i -= nq;
+            if (i < nd) { v[j] = srcd[i]; continue; }
+            i -= nd;
+            if (i < ng) { v[j] = srcg[i]; continue; }
+            v[j] = srcs[i - ng];
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t i = base + j * blockDim.x + threadIdx.x;
+            if (i >= n) continue;
+            if (i < nq) { dq[act_swizzle(i)] = v[j]; continue; }
+            i -= nq;
+            if (i < nd) { dd[i] = v[j]; continue; }
+            i -= nd;
+            if (i < ng) { dg[i] = v[j]; continue; }
+            ds[i - ng] = v[j];
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kGemvThreads, 1) moe_gemv_kernel(MoeArgs a) {
@@ -212,41 +300,48 @@ __global__ void __launch_bounds__(kGemvThreads, 1) moe_gemv_kernel(MoeArgs a) {
     const int KB = a.K >> 5;
     const int rowbytes = KB * 10;
     const int RG = kConsumerWarps / a.WK;
-    Ring r = carve_ring(smem, a.nstages, RG * rowbytes, RG, a.WK, NextPow2<kGroupCols>::v);
+    Ring r = carve_ring(smem, a.nstages, RG * kRows * rowbytes, RG, a.WK,
+                        NextPow2<kRows * kGroupCols>::v);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t qbytes = (uint32_t)a.T * a.K, dbytes = (uint32_t)a.T * KB * 4;
-    uint8_t *act_q = smem + ring_bytes(a.nstages, RG * rowbytes, RG, a.WK, NextPow2<kGroupCols>::v);
+    const uint32_t qbytes = a.act_staged ? (uint32_t)a.T * a.K : 0;
+    const uint32_t dbytes = a.act_staged ? (uint32_t)a.T * KB * 4 : 0;
+    uint8_t *act_q = smem + ring_bytes(a.nstages, RG * kRows * rowbytes, RG, a.WK,
+                                       NextPow2<kRows * kGroupCols>::v);
     uint8_t *act_d = act_q + ((qbytes + 15) & ~15u);
+    int4 *sgroups = reinterpret_cast<int4 *>(act_d + ((dbytes + 15) & ~15u));
+    int *ssorted = reinterpret_cast<int *>(sgroups + (a.meta_staged ? a.T * a.top_k : 0));
     if (threadIdx.x == kConsumerWarps * 32) init_ring_stages(r, kConsumerWarps);
     init_ring_reduction(r, threadIdx.x, kConsumerWarps * 32);
-    __syncthreads();
     // the group list and the quantized tokens come from the two launches before
     pdl_wait();
     pdl_launch_dependents();
-    if (a.act_staged && warp == kConsumerWarps)
-        load_act_to_smem(r, lane, act_q, a.ws.q, qbytes, act_d, a.ws.d, dbytes);
     const int ngroups = a.ws.header[0];
+    const int nvalid = a.ws.header[1];
+    stage_inputs(a, ngroups, nvalid, act_q, act_d, sgroups, ssorted);
+    __syncthreads();
+    const int4 *groups = a.meta_staged ? sgroups : a.ws.groups;
+    const int *sorted = a.meta_staged ? ssorted : a.ws.sorted;
     const int tiles = (a.M + a.tile_rows - 1) / a.tile_rows;
     // units (group, row tile) split into contiguous, balanced CTA ranges
     const int units = ngroups * tiles;
     const int per = units / (int)gridDim.x, extra = units % (int)gridDim.x;
     const int bx = blockIdx.x;
-    const int64_t u0 = (int64_t)bx * per + min(bx, extra);
-    const int64_t u1 = u0 + per + (bx < extra ? 1 : 0);
+    const int u0 = bx * per + min(bx, extra);
+    const int u1 = u0 + per + (bx < extra ? 1 : 0);
 
     if (warp == kConsumerWarps) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             int c = 0;
             bool ok = true;
-            for (int64_t u = u0; u < u1 && ok; ++u) {
-                const int g = (int)(u / tiles), t = (int)(u % tiles);
-                const int4 grp = a.ws.groups[g];
+            for (int u = u0; u < u1 && ok; ++u) {
+                const int g = u / tiles, t = u - g * tiles;
+                const int4 grp = groups[g];
                 const uint8_t *base = a.W + (int64_t)grp.x * a.expert_bytes;
                 const int r0 = t * a.tile_rows;
                 const int r1 = min(a.M, r0 + a.tile_rows);
-                for (int row = r0; row < r1 && ok; row += RG, ++c) {
-                    const int rows = min(RG, r1 - row);
+                for (int row = r0; row < r1 && ok; row += RG * kRows, ++c) {
+                    const int rows = min(RG * kRows, r1 - row);
                     ok = produce_chunk(r, c, base + (int64_t)row * rowbytes,
                                        (uint32_t)(rows * rowbytes), pol, a.status);
                     if (!ok) break;
@@ -260,31 +355,36 @@ __global__ void __launch_bounds__(kGemvThreads, 1) moe_gemv_kernel(MoeArgs a) {
     const int wg = warp / a.WK, wk = warp % a.WK;
     const int kb0 = (wk * 32 + lane) * kBpt;
     const bool active = kb0 < KB;
-    const int8_t *q = a.ws.q;
-    const float *d = a.ws.d;
-    if (a.act_staged) {
-        if (!mbar_wait(r.act_bar, 0)) {
-            record_status(a.status, RFP2_ETIMEOUT);
-            *r.abort_flag = 1;
-            return;
-        }
-        q = reinterpret_cast<const int8_t *>(act_q);
-        d = reinterpret_cast<const float *>(act_d);
-    }
+    const int8_t *q = a.act_staged ? reinterpret_cast<const int8_t *>(act_q) : a.ws.q;
+    const float *d = a.act_staged ? reinterpret_cast<const float *>(act_d) : a.ws.d;
     int c = 0;
-    int64_t u = u0;
+    int u = u0;
     while (u < u1) {
-        const int g = (int)(u / tiles);
-        const int t_begin = (int)(u % tiles);
-        int64_t u_end = min(u1, (int64_t)(g + 1) * tiles);
-        const int t_end = (int)(u_end - (int64_t)g * tiles);
-        const int4 grp = a.ws.groups[g];
+        const int g = u / tiles;
+        const int t_begin = u - g * tiles;
+        const int u_end = min(u1, (g + 1) * tiles);
+        const int t_end = u_end - g * tiles;
+        const int4 grp = groups[g];
         bool ok = true;
-        switch (grp.z) {
-            case 1: ok = consume_group<1>(r, a, grp, t_begin, t_end, c, wg, a.WK > 1 ? wk : 0, lane, kb0, active, rowbytes, q, d, a.act_staged != 0); break;
-            case 2: ok = consume_group<2>(r, a, grp, t_begin, t_end, c, wg, a.WK > 1 ? wk : 0, lane, kb0, active, rowbytes, q, d, a.act_staged != 0); break;
-            case 3: ok = consume_group<3>(r, a, grp, t_begin, t_end, c, wg, a.WK > 1 ? wk : 0, lane, kb0, active, rowbytes, q, d, a.act_staged != 0); break;
-            default: ok = consume_group<4>(r, a, grp, t_begin, t_end, c, wg, a.WK > 1 ? wk : 0, lane, kb0, active, rowbytes, q, d, a.act_staged != 0); break;
+        const int wkk = a.WK > 1 ? wk : 0;
+        if (kGroupCols >= 2 && grp.z >= 2) {
+            if constexpr (kGroupCols >= 4) {
+                if (grp.z == 4)
+                    ok = consume_group<4>(r, a, grp, t_begin, t_end, c, wg, wkk, lane, kb0, active,
+                                          rowbytes, q, d, a.act_staged != 0, sorted);
+                else if (grp.z == 3)
+                    ok = consume_group<3>(r, a, grp, t_begin, t_end, c, wg, wkk, lane, kb0, active,
+                                          rowbytes, q, d, a.act_staged != 0, sorted);
+                else
+                    ok = consume_group<2>(r, a, grp, t_begin, t_end, c, wg, wkk, lane, kb0, active,
+                                          rowbytes, q, d, a.act_staged != 0, sorted);
+            } else {
+                ok = consume_group<2>(r, a, grp, t_begin, t_end, c, wg, wkk, lane, kb0, active,
+                                      rowbytes, q, d, a.act_staged != 0, sorted);
+            }
+        } else {
+            ok = consume_group<1>(r, a, grp, t_begin, t_end, c, wg, wkk, lane, kb0, active,
+                                  rowbytes, q, d, a.act_staged != 0, sorted);
         }
         if (!ok) break;
         u = u_end;
@@ -292,11 +392,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1) moe_gemv_kernel(MoeArgs a) {
 }
 
 struct MoePlan {
-    int WK, RG, nstages, tile_rows, grid, act_staged;
+    int WK, RG, nstages, tile_rows, grid, act_staged, meta_staged;
     size_t smem;
 };
 
-bool make_moe_plan(int64_t T, int64_t M, int64_t K, MoePlan &p) {
+bool make_moe_plan(int64_t T, int64_t top_k, int64_t M, int64_t K, MoePlan &p) {
     const int KB = (int)(K / 32);
     int WK = (KB + 32 * kBpt - 1) / (32 * kBpt);
     int WKp = 1;
@@ -304,14 +404,17 @@ bool make_moe_plan(int64_t T, int64_t M, int64_t K, MoePlan &p) {
     if (WKp > kConsumerWarps) return false;
     p.WK = WKp;
     p.RG = kConsumerWarps / WKp;
-    p.tile_rows = p.RG * kChunksPerTile;
-    const int chunk_bytes = p.RG * KB * 10;
-    const int V = NextPow2<kGroupCols>::v;
+    p.tile_rows = p.RG * kRows * kChunksPerTile;
+    const int chunk_bytes = p.RG * kRows * KB * 10;
+    const int V = NextPow2<kRows * kGroupCols>::v;
     // stage every token's quantized activations in shared memory when they fit
     const size_t act = ((size_t)T * K + 15) / 16 * 16 + (size_t)T * KB * 4;
     p.act_staged = act <= 96 * 1024;
-    const size_t act_smem = p.act_staged ? act : 0;
-    int stages = 16;
+    // the group list (<= T*top_k int4) and the pair order (T*top_k ints)
+    const size_t meta = (size_t)T * top_k * 16 + ((size_t)T * top_k * 4 + 15) / 16 * 16;
+    p.meta_staged = meta <= 16 * 1024;
+    const size_t act_smem = (p.act_staged ? act : 0) + (p.meta_staged ? meta : 0);
+    int stages = 32;
     while (stages > 1 &&
            ring_bytes(stages, chunk_bytes, p.RG, p.WK, V) + act_smem > (size_t)kGemvSmemBudget)
         --stages;
@@ -341,28 +444,31 @@ extern "C" rfp2_status rfp2_moe_gemv(const uint8_t *W, int64_t E, int64_t M, int
         return RFP2_ESHAPE;
     if (K % 256 != 0) return RFP2_EUNSUPPORTED;
     MoePlan p;
-    if (!make_moe_plan(T, M, K, p)) return RFP2_EUNSUPPORTED;
+    if (!make_moe_plan(T, top_k, M, K, p)) return RFP2_EUNSUPPORTED;
     if (!workspace || workspace_bytes < moe_ws_bytes(T, top_k, K)) return RFP2_EWORKSPACE;
     if (!aligned(W, 16) || !aligned(x, 4) || !aligned(y, 4) || !aligned(ids, 4) ||
         !aligned(workspace, 256))
         return RFP2_EALIGN;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     MoeWs w = carve_ws(workspace, T, top_k, K);
-    cudaError_t e = launch(moe_route_kernel, dim3(1), dim3(kRouteThreads), 0, s, true, ids,
-                           (int)(T * top_k), E, (int)M, y, dev_status, w);
-    if (e != cudaSuccess) return RFP2_ECUDA;
-    e = launch_quantize(x, T, K, w.q, w.d, s, true);
-    if (e != cudaSuccess) return RFP2_ECUDA;
     static std::mutex mu;
     static int configured[64] = {0};
     const int dev = current_device();
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 64 && !configured[dev]) {
-            if (set_smem_limit(moe_gemv_kernel, 227 * 1024) != cudaSuccess) return RFP2_ECUDA;
+            if (set_smem_limit(moe_gemv_kernel, 227 * 1024) != cudaSuccess ||
+                set_smem_limit(moe_route_kernel, (int)route_smem_bytes(kMaxPairs)) != cudaSuccess)
+                return RFP2_ECUDA;
             configured[dev] = 1;
         }
     }
+    cudaError_t e = launch(moe_route_kernel, dim3(1), dim3(kRouteThreads),
+                           route_smem_bytes((int)(T * top_k)), s, true, ids, (int)(T * top_k), E,
+                           (int)M, y, dev_status, w);
+    if (e != cudaSuccess) return RFP2_ECUDA;
+    e = launch_quantize(x, T, K, w.q, w.d, s, true);
+    if (e != cudaSuccess) return RFP2_ECUDA;
     MoeArgs a;
     a.W = W;
     a.expert_bytes = M * (K / 32) * 10;
@@ -371,6 +477,7 @@ extern "C" rfp2_status rfp2_moe_gemv(const uint8_t *W, int64_t E, int64_t M, int
     a.T = (int)T;
     a.top_k = (int)top_k;
     a.act_staged = p.act_staged;
+    a.meta_staged = p.meta_staged;
     a.WK = p.WK;
     a.nstages = p.nstages;
     a.tile_rows = p.tile_rows;
