@@ -7,12 +7,13 @@
 // "Nibble packing"; the page's correctness-anchor loop is the oracle.
 //
 // GB300 design (the page's kernels are RDNA v_ldexp/WMMA code):
-//  * E2M1 codes are exact in f16, so each 32-weight block is one pair of
+//  * E2M1 codes are exact in f16, so each 32-weight block is two k-steps of
 //    m16n8k16 f16 MMAs per row tile with a fresh fp32 accumulator, scaled by
-//    2^(e-127) in the epilogue (the block exponent varies per row and block,
-//    so it cannot be folded into the accumulation).  The N <= 8 activation
-//    columns are the MMA's n dimension, so the weight decode (one E2M1x2 ->
-//    f16x2 conversion per two weights) is shared by all columns.
+//    2^(e-127) (the block exponent varies per row and block, so it cannot be
+//    folded into the accumulation).  The activation columns are the MMA's n
+//    dimension, so the weight decode (one E2M1x2 -> f16x2 conversion per two
+//    weights) is shared by all columns; for N <= 4 both f16 pieces of every
+//    token fit in the eight columns and one MMA per k-step does the block.
 //  * fp32 activations are made exact enough for f16 by a prep kernel: each
 //    column is scaled by a power of two 2^-kc (max |x| -> [1, 2)) and split
 //    into two f16 pieces x' ~= hi + lo (relative residual <= 2^-22); both
@@ -20,8 +21,8 @@
 //    end.  The prep kernel writes the pieces in MMA fragment order.
 //  * Weights stream through 2-D TMA tiles of 64 rows x 1024 K (544 bytes per
 //    row; rows past M and columns past the row are zero-filled), with the
-//    matching activation fragments, into a 3-4 stage ring; eight consumer
-//    warps each take 4 of the 32 blocks of a tile, and their partial sums are
+//    matching activation fragments, into a 3-4 stage ring; sixteen consumer
+//    warps each take 2 of the 32 blocks of a tile, and their partial sums are
 //    combined in shared memory.  All waits are bounded.
 #include <cuda_fp16.h>
 
@@ -39,7 +40,11 @@ constexpr int kRows = kTile * kMaxTiles; // 64 rows per stage
 constexpr int kChunkBlocks = 32;         // 1024 K per stage
 constexpr int kChunkRowBytes = kChunkBlocks * 17;  // 544
 constexpr int kWStageBytes = kRows * kChunkRowBytes;  // 34816
-constexpr int kWarps = 8;                // consumer warps, 4 blocks each
+#ifndef RFP2_HFP4_WARPS
+#define RFP2_HFP4_WARPS 16
+#endif
+constexpr int kWarps = RFP2_HFP4_WARPS;  // consumer warps
+constexpr int kBlocksPerWarp = kChunkBlocks / kWarps;  // blocks of a chunk per warp
 constexpr int kThreads = (kWarps + 1) * 32;
 constexpr int kRedBytes = kWarps * kMaxTiles * 32 * 16;
 
@@ -91,11 +96,15 @@ __global__ void __launch_bounds__(256) hfp4_split_kernel(const float *__restrict
     }
 }
 
-// Two E2M1 codes (low nibble = even element) -> f16x2 (low half = even).
-__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
-    uint32_t h;
-    asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(h) : "r"(byte));
-    return h;
+// Eight E2M1 codes (four bytes; in each byte the low nibble is the even
+// element) -> four f16x2 words (low half = even element).
+__device__ __forceinline__ void e2m1x8_to_h2x4(uint32_t w, uint32_t &h0, uint32_t &h1,
+                                               uint32_t &h2, uint32_t &h3) {
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+        : "r"(w));
 }
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -132,6 +141,10 @@ struct HfpArgs {
     const uint4 *frag;
 };
 
+// PAIRED (N <= 4): the two f16 pieces of token n are MMA columns 2n and
+// 2n + 1, so one MMA per k-step covers both; otherwise the columns are the
+// tokens and each piece takes its own MMA.
+template <bool PAIRED>
 __global__ void __launch_bounds__(kThreads, 1)
     hfp4_gemv_kernel(const __grid_constant__ CUtensorMap wmap, HfpArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -154,6 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nchunks = (KB + kChunkBlocks - 1) / kChunkBlocks;
     const int nks = a.K / 16;
 
+    // 2^(e-127) for every UE8M0 byte (0 -> 2^-127, 0xFF -> NaN)
+    __shared__ float scale_lut[256];
+    for (int e = threadIdx.x; e < 256; e += blockDim.x) scale_lut[e] = ue8m0((uint32_t)e);
     if (threadIdx.x == kWarps * 32) {
         prefetch_tensor_map(&wmap);
         for (int s = 0; s < S; ++s) {
@@ -228,13 +244,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t *ws = wst + (size_t)s * kWStageBytes;
         const uint4 *bs = reinterpret_cast<const uint4 *>(bst + (size_t)s * bstage_bytes);
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            const int j = warp * 4 + jj;  // block inside the chunk
+        for (int jj = 0; jj < kBlocksPerWarp; ++jj) {
+            const int j = warp * kBlocksPerWarp + jj;  // block inside the chunk
             if (c * kChunkBlocks + j >= KB) break;
+            uint32_t b[4] = {0u, 0u, 0u, 0u};  // k-step 0 (b[0], b[1]), k-step 1 (b[2], b[3])
+            if constexpr (PAIRED) {
+                const int n = g >> 1;
+                if (n < a.N) {
+                    const uint4 t0 = bs[((2 * j) * a.N + n) * 4 + p];
+                    const uint4 t1 = bs[((2 * j + 1) * a.N + n) * 4 + p];
+                    const bool lo = (g & 1) != 0;
+                    b[0] = lo ? t0.z : t0.x;
+                    b[1] = lo ? t0.w : t0.y;
+                    b[2] = lo ? t1.z : t1.x;
+                    b[3] = lo ? t1.w : t1.y;
+                }
+            }
             uint4 b0 = make_uint4(0, 0, 0, 0), b1 = make_uint4(0, 0, 0, 0);
-            if (g < a.N) {
-                b0 = bs[((2 * j) * a.N + g) * 4 + p];
-                b1 = bs[((2 * j + 1) * a.N + g) * 4 + p];
+            if constexpr (!PAIRED) {
+                if (g < a.N) {
+                    b0 = bs[((2 * j) * a.N + g) * 4 + p];
+                    b1 = bs[((2 * j + 1) * a.N + g) * 4 + p];
+                }
             }
 #pragma unroll
             for (int t = 0; t < kMaxTiles; ++t) {
@@ -245,19 +276,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t wb = load_u32_unaligned(rbp + 1 + 4 * p);
                     float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                     // k-step 0: bytes 0,1 of the word; k-step 1: bytes 2,3
-                    const uint32_t a0 = e2m1x2_to_h2(wa), a1 = e2m1x2_to_h2(wb);
-                    const uint32_t a2 = e2m1x2_to_h2(wa >> 8), a3 = e2m1x2_to_h2(wb >> 8);
-                    mma_f16(d, a0, a1, a2, a3, b0.x, b0.y);
-                    mma_f16(d, a0, a1, a2, a3, b0.z, b0.w);
-                    const uint32_t a4 = e2m1x2_to_h2(wa >> 16), a5 = e2m1x2_to_h2(wb >> 16);
-                    const uint32_t a6 = e2m1x2_to_h2(wa >> 24), a7 = e2m1x2_to_h2(wb >> 24);
-                    mma_f16(d, a4, a5, a6, a7, b1.x, b1.y);
-                    mma_f16(d, a4, a5, a6, a7, b1.z, b1.w);
-                    const float sa = ue8m0(ra[0]), sb = ue8m0(rbp[0]);
-                    acc[t][0] = fmaf(d[0], sa, acc[t][0]);
-                    acc[t][1] = fmaf(d[1], sa, acc[t][1]);
-                    acc[t][2] = fmaf(d[2], sb, acc[t][2]);
-                    acc[t][3] = fmaf(d[3], sb, acc[t][3]);
+                    uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
+                    e2m1x8_to_h2x4(wa, a0, a2, a4, a6);
+                    e2m1x8_to_h2x4(wb, a1, a3, a5, a7);
+                    const float sa = scale_lut[ra[0]], sb = scale_lut[rbp[0]];
+                    if constexpr (PAIRED) {
+                        mma_f16(d, a0, a1, a2, a3, b[0], b[1]);
+                        mma_f16(d, a4, a5, a6, a7, b[2], b[3]);
+                        // columns 2p, 2p+1 = the two pieces of token p
+                        acc[t][0] = fmaf(d[0] + d[1], sa, acc[t][0]);
+                        acc[t][1] = fmaf(d[2] + d[3], sb, acc[t][1]);
+                    } else {
+                        mma_f16(d, a0, a1, a2, a3, b0.x, b0.y);
+                        mma_f16(d, a0, a1, a2, a3, b0.z, b0.w);
+                        mma_f16(d, a4, a5, a6, a7, b1.x, b1.y);
+                        mma_f16(d, a4, a5, a6, a7, b1.z, b1.w);
+                        acc[t][0] = fmaf(d[0], sa, acc[t][0]);
+                        acc[t][1] = fmaf(d[1], sa, acc[t][1]);
+                        acc[t][2] = fmaf(d[2], sb, acc[t][2]);
+                        acc[t][3] = fmaf(d[3], sb, acc[t][3]);
+                    }
                 }
             }
         }
@@ -277,9 +315,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
     if (!ok) return;
-    const int c0 = 2 * p, c1 = 2 * p + 1;
-    const float s0 = c0 < a.N ? ldexpf(1.0f, a.kc[c0]) : 0.0f;
-    const float s1 = c1 < a.N ? ldexpf(1.0f, a.kc[c1]) : 0.0f;
     for (int t = 0; t < ntiles; ++t) {
         float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         for (int w = 0; w < kWarps; ++w) {
@@ -290,15 +325,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[3] += q.w;
         }
         const int r0 = row0 + t * kTile + g, r1 = r0 + 8;
-        if (r0 < a.M) {
-            const float rs = __half2float(*reinterpret_cast<const __half *>(a.W + (int64_t)r0 * a.rb));
-            if (c0 < a.N) a.y[(int64_t)c0 * a.M + r0] = v[0] * rs * s0;
-            if (c1 < a.N) a.y[(int64_t)c1 * a.M + r0] = v[1] * rs * s1;
-        }
-        if (r1 < a.M) {
-            const float rs = __half2float(*reinterpret_cast<const __half *>(a.W + (int64_t)r1 * a.rb));
-            if (c0 < a.N) a.y[(int64_t)c0 * a.M + r1] = v[2] * rs * s0;
-            if (c1 < a.N) a.y[(int64_t)c1 * a.M + r1] = v[3] * rs * s1;
+        const float rs0 =
+            r0 < a.M ? __half2float(*reinterpret_cast<const __half *>(a.W + (int64_t)r0 * a.rb)) : 0.0f;
+        const float rs1 =
+            r1 < a.M ? __half2float(*reinterpret_cast<const __half *>(a.W + (int64_t)r1 * a.rb)) : 0.0f;
+        if constexpr (PAIRED) {
+            if (p < a.N) {
+                const float s0 = ldexpf(1.0f, a.kc[p]);
+                if (r0 < a.M) a.y[(int64_t)p * a.M + r0] = v[0] * rs0 * s0;
+                if (r1 < a.M) a.y[(int64_t)p * a.M + r1] = v[1] * rs1 * s0;
+            }
+        } else {
+            const int c0 = 2 * p, c1 = 2 * p + 1;
+            const float s0 = c0 < a.N ? ldexpf(1.0f, a.kc[c0]) : 0.0f;
+            const float s1 = c1 < a.N ? ldexpf(1.0f, a.kc[c1]) : 0.0f;
+            if (r0 < a.M) {
+                if (c0 < a.N) a.y[(int64_t)c0 * a.M + r0] = v[0] * rs0 * s0;
+                if (c1 < a.N) a.y[(int64_t)c1 * a.M + r0] = v[1] * rs0 * s1;
+            }
+            if (r1 < a.M) {
+                if (c0 < a.N) a.y[(int64_t)c0 * a.M + r1] = v[2] * rs1 * s0;
+                if (c1 < a.N) a.y[(int64_t)c1 * a.M + r1] = v[3] * rs1 * s1;
+            }
         }
     }
 }
@@ -337,7 +385,7 @@ extern "C" rfp2_status hfp4_gemv(const uint8_t *W, int64_t M, int64_t K, const f
     // stages: as many 64-row x 1024-K tiles (plus their fragments) as fit
     const size_t per_stage = kWStageBytes + (size_t)64 * N * 64;
     int stages = 4;
-    while (stages > 2 && stages * per_stage + kRedBytes + 256 > 227 * 1024) --stages;
+    while (stages > 2 && stages * per_stage + kRedBytes + 256 > 226 * 1024) --stages;
     const size_t smem = stages * per_stage + kRedBytes + 256;
     static std::mutex mu;
     static int configured[64] = {0};
@@ -345,7 +393,9 @@ extern "C" rfp2_status hfp4_gemv(const uint8_t *W, int64_t M, int64_t K, const f
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 64 && !configured[dev]) {
-            if (set_smem_limit(hfp4_gemv_kernel, 227 * 1024) != cudaSuccess) return RFP2_ECUDA;
+            if (set_smem_limit(hfp4_gemv_kernel<true>, 226 * 1024) != cudaSuccess ||
+                set_smem_limit(hfp4_gemv_kernel<false>, 226 * 1024) != cudaSuccess)
+                return RFP2_ECUDA;
             configured[dev] = 1;
         }
     }
@@ -366,5 +416,9 @@ extern "C" rfp2_status hfp4_gemv(const uint8_t *W, int64_t M, int64_t K, const f
     a.status = dev_status;
     a.kc = kc;
     a.frag = frag;
-    return from_cuda(launch(hfp4_gemv_kernel, dim3(grid), dim3(kThreads), smem, s, true, wmap, a));
+    if (N <= 4)
+        return from_cuda(
+            launch(hfp4_gemv_kernel<true>, dim3(grid), dim3(kThreads), smem, s, true, wmap, a));
+    return from_cuda(
+        launch(hfp4_gemv_kernel<false>, dim3(grid), dim3(kThreads), smem, s, true, wmap, a));
 }
