@@ -441,6 +441,23 @@ def secondary(torch, gl, peaks):
         "bound": "tensor", "peak_source": peaks["source"] + " bf16_tflops (cuBLAS bf16)"}
     del P, X, Y, ws
     torch.cuda.empty_cache()
+
+    # HFP4G32 prefill GEMM on the same shapes (expansion to bf16 included)
+    P = gl.hfp4_pack_weights(torch.from_numpy(w["W"]).cuda())
+    X = torch.from_numpy(w["X"].view(np.int16)).cuda()
+    Y = torch.empty((N, M), dtype=torch.float32, device="cuda")
+    ws = torch.empty(gl.hfp4_gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    us = _graph_us(torch, lambda i: gl.hfp4_gemm(P, M, K, X, Y=Y, workspace=ws), 20, 3)
+    tflops = 2.0 * M * K * N / us / 1e6
+    out["hfp4_prefill_gemm"] = {
+        "workload": "HFP4G32 [17408, 5120] N(0, 0.015^2) x bf16 [2048, 5120] (0.5% x20), seed 3",
+        "value": round(tflops, 1), "unit": "TFLOP/s (2*M*N*K, expansion included)",
+        "us_per_call": round(us, 1),
+        "frac_of_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),
+        "frac_of_bf16_sustained": round(tflops / peaks["bf16_tflops_sustained"], 4),
+        "bound": "tensor", "peak_source": peaks["source"] + " bf16_tflops (cuBLAS bf16)"}
+    del P, X, Y, ws
+    torch.cuda.empty_cache()
     return out
 
 

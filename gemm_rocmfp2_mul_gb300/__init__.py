@@ -62,6 +62,8 @@ _SIGNATURES = {
     "rfp2_moe_gemv": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _P, _SZ, _P, _P]),
     "rfp2_gemm_workspace_bytes": (_SZ, [_I64, _I64]),
     "rfp2_gemm": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
+    "hfp4_gemm_workspace_bytes": (_SZ, [_I64, _I64]),
+    "hfp4_gemm": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
     "hfp4_gemv_workspace_bytes": (_SZ, [_I64, _I64]),
     "hfp4_gemv": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
     "rfp2_pack_weights": (_I32, [_P, _I64, _I64, _P, _P]),
@@ -245,6 +247,27 @@ def rfp2_gemm(W, M, K, X, Y=None, workspace=None, dev_status=None):
     ws = _workspace(workspace, rfp2_gemm_workspace_bytes(M, K), X)
     _check(lib().rfp2_gemm(_ptr(W), M, K, _ptr(X), N, _ptr(Y), _ptr(ws), ws.numel(),
                            _ptr(dev_status), _stream()), "rfp2_gemm")
+    return Y
+
+
+def hfp4_gemm_workspace_bytes(M: int, K: int) -> int:
+    return int(lib().hfp4_gemm_workspace_bytes(M, K))
+
+
+def hfp4_gemm(W, M, K, X, Y=None, workspace=None, dev_status=None):
+    """HFP4G32 prefill GEMM on tensor cores: Y fp32 [N, M] = X (bf16 [N, K]) W^T."""
+    torch = _torch()
+    _need(W, torch.uint8, "W")
+    if X.dtype == torch.bfloat16:
+        X = X.view(torch.int16)
+    if X.dtype not in (torch.int16, torch.uint16):
+        raise TypeError("X must be bfloat16 (or its 16-bit pattern)")
+    _need(X, X.dtype, "X")
+    N = X.shape[0]
+    Y = _empty((N, M), torch.float32, X) if Y is None else _need(Y, torch.float32, "Y")
+    ws = _workspace(workspace, hfp4_gemm_workspace_bytes(M, K), X)
+    _check(lib().hfp4_gemm(_ptr(W), M, K, _ptr(X), N, _ptr(Y), _ptr(ws), ws.numel(),
+                           _ptr(dev_status), _stream()), "hfp4_gemm")
     return Y
 
 

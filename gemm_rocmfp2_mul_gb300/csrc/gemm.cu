@@ -9,7 +9,9 @@
 //
 // Two launches:
 //  1. expand: packed 10-byte blocks -> bf16 rows in the workspace (one thread
-//     per 32-weight block, 64 bytes written per block).
+//     per 32-weight block, 64 bytes written per block).  The HFP4G32 variant
+//     (hfp4_gemm) expands E2M1 x 2^(e-127) the same way and leaves the f16
+//     row scale to the GEMM's epilogue.
 //  2. gemm: one CTA per 128-token x 256-weight-row tile.  Warp 0 loads
 //     K-major 64-element slices of both operands with 2-D TMA (SWIZZLE_128B)
 //     into a 4-stage ring; one thread of warp 1 issues tcgen05.mma kind::f16
@@ -71,10 +73,62 @@ __global__ void __launch_bounds__(256) expand_bf16_kernel(const uint8_t *__restr
     }
 }
 
+// HFP4G32 rows -> bf16: element = E2M1[c] * 2^(e-127) (at most two
+// significant bits times a power of two: exact in bf16, including the
+// subnormal range; block byte 0xFF gives NaN), and the row scale row_scale_a
+// (f16) as fp32, applied by the GEMM's epilogue.  One thread per 32-weight
+// block; HFP4 "Element format (OCP E2M1)", "Block scale - UE8M0",
+// "Per-row second-level scale (FP16)", "Byte layout - HFP4G32".
+__global__ void __launch_bounds__(256) hfp4_expand_bf16_kernel(const uint8_t *__restrict__ W,
+                                                               int M, int KB, int rb,
+                                                               __nv_bfloat16 *__restrict__ out,
+                                                               float *__restrict__ rs32) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= (int64_t)M * KB) return;
+    const int64_t m = j / KB;
+    const int b = (int)(j - m * KB);
+    const uint8_t *row = W + m * rb;
+    if (b == 0) rs32[m] = __half2float(__ushort_as_half((unsigned short)(row[0] | (row[1] << 8))));
+    // the 17-byte block lies inside five aligned words (rows are 4-byte
+    // aligned because K % 256 == 0): byte t of the block is byte t of u
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(row + 16 + 17 * b);
+    const uint32_t *wp = reinterpret_cast<const uint32_t *>(addr & ~uintptr_t(3));
+    const uint32_t sh = (uint32_t)(addr & 3) * 8;
+    uint32_t v[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) v[i] = __ldg(wp + i);
+    uint32_t u[5];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) u[i] = __funnelshift_r(v[i], v[i + 1], sh);
+    u[4] = v[4] >> sh;
+    const uint32_t e = u[0] & 0xFFu;
+    const float sc = __uint_as_float(e == 0 ? 0x00400000u : e == 0xFF ? 0x7FC00000u : e << 23);
+    const float mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+    uint4 *o = reinterpret_cast<uint4 *>(out + j * 32);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // 8 weights (code bytes 1+4q .. 4+4q) per 16-byte store
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = 1 + 4 * q + i;  // byte of the block
+            const uint32_t byte = (u[t >> 2] >> (8 * (t & 3))) & 0xFFu;
+            const uint32_t c0 = byte & 15, c1 = byte >> 4;
+            const float f0 = (c0 & 8 ? -mag[c0 & 7] : mag[c0 & 7]) * sc;
+            const float f1 = (c1 & 8 ? -mag[c1 & 7] : mag[c1 & 7]) * sc;
+            w[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f0)) |
+                   ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f1)) << 16);
+        }
+        o[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 // ---- GEMM --------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-                     float *__restrict__ Y, int Ntok, int Mw, int K, int32_t *status) {
+                     float *__restrict__ Y, int Ntok, int Mw, int K, const float *__restrict__ colscale,
+                     int32_t *status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -166,10 +220,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float4 *dst = reinterpret_cast<float4 *>(Y + (int64_t)row * Mw + col0);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        if (col0 + 4 * i < Mw)
-                            dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                                 __uint_as_float(r[4 * i + 2]),
-                                                 __uint_as_float(r[4 * i + 3]));
+                        if (col0 + 4 * i < Mw) {
+                            float4 v = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                   __uint_as_float(r[4 * i + 2]),
+                                                   __uint_as_float(r[4 * i + 3]));
+                            if (colscale) {  // per weight row (e.g. HFP4's row_scale_a)
+                                const float4 cs =
+                                    *reinterpret_cast<const float4 *>(colscale + col0 + 4 * i);
+                                v.x *= cs.x;
+                                v.y *= cs.y;
+                                v.z *= cs.z;
+                                v.w *= cs.w;
+                            }
+                            dst[i] = v;
+                        }
                 }
             }
         }
@@ -200,7 +264,7 @@ extern "C" rfp2_status rfp2_gemm(const uint8_t *W, int64_t M, int64_t K, const u
     if (M > (1LL << 30) || N > (1LL << 30) || K > (1 << 20)) return RFP2_ESHAPE;
     if (K % 256 != 0 || M % 16 != 0) return RFP2_EUNSUPPORTED;
     if (!workspace || workspace_bytes < (size_t)M * K * 2) return RFP2_EWORKSPACE;
-    if (!aligned(W, 16) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(workspace, 1024))
+    if (!aligned(W, 16) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(workspace, 256))
         return RFP2_EALIGN;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     __nv_bfloat16 *wexp = static_cast<__nv_bfloat16 *>(workspace);
@@ -226,5 +290,59 @@ extern "C" rfp2_status rfp2_gemm(const uint8_t *W, int64_t M, int64_t K, const u
     }
     const dim3 grid((unsigned)((N + BM - 1) / BM), (unsigned)((M + BN - 1) / BN));
     return from_cuda(launch(gemm_bf16_kernel, grid, dim3(kThreads), kSmemBytes, s, true, xmap, wmap,
-                            Y, (int)N, (int)M, (int)K, dev_status));
+                            Y, (int)N, (int)M, (int)K, static_cast<const float *>(nullptr),
+                            dev_status));
+}
+
+// ---- HFP4G32 prefill GEMM ------------------------------------------------------
+
+static size_t hfp4_gemm_ws(int64_t M, int64_t K) {
+    return ((size_t)M * K * 2 + 255) / 256 * 256 + (size_t)M * 4;
+}
+
+extern "C" size_t hfp4_gemm_workspace_bytes(int64_t M, int64_t K) {
+    if (M <= 0 || K <= 0) return 0;
+    return hfp4_gemm_ws(M, K);
+}
+
+extern "C" rfp2_status hfp4_gemm(const uint8_t *W, int64_t M, int64_t K, const uint16_t *X,
+                                 int64_t N, float *Y, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, rfp2_stream_t stream) {
+    if (!W || !X || !Y) return RFP2_EINVAL;
+    if (M <= 0 || K <= 0 || N <= 0) return RFP2_ESHAPE;
+    if (M > (1LL << 30) || N > (1LL << 30) || K > (1 << 20)) return RFP2_ESHAPE;
+    if (K % 256 != 0 || M % 16 != 0) return RFP2_EUNSUPPORTED;
+    if (!workspace || workspace_bytes < hfp4_gemm_ws(M, K)) return RFP2_EWORKSPACE;
+    if (!aligned(W, 16) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(workspace, 256))
+        return RFP2_EALIGN;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    __nv_bfloat16 *wexp = static_cast<__nv_bfloat16 *>(workspace);
+    float *rs32 = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                            ((size_t)M * K * 2 + 255) / 256 * 256);
+    const int KB = (int)(K / 32);
+    const int rb = (int)(16 + 17 * KB);
+    const int64_t nblocks = M * KB;
+    cudaError_t e = launch(hfp4_expand_bf16_kernel, dim3((unsigned)((nblocks + 255) / 256)),
+                           dim3(256), 0, s, true, W, (int)M, KB, rb, wexp, rs32);
+    if (e != cudaSuccess) return RFP2_ECUDA;
+    CUtensorMap xmap, wmap;
+    if (!encode_tensor_map_2d(&xmap, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K, (uint64_t)N,
+                              (uint64_t)K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_2d(&wmap, wexp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K,
+                              (uint64_t)M, (uint64_t)K * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return RFP2_ECUDA;
+    static std::mutex mu;
+    static int configured[64] = {0};
+    const int dev = current_device();
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && !configured[dev]) {
+            if (set_smem_limit(gemm_bf16_kernel, (int)kSmemBytes) != cudaSuccess) return RFP2_ECUDA;
+            configured[dev] = 1;
+        }
+    }
+    const dim3 grid((unsigned)((N + BM - 1) / BM), (unsigned)((M + BN - 1) / BN));
+    return from_cuda(launch(gemm_bf16_kernel, grid, dim3(kThreads), kSmemBytes, s, true, xmap, wmap,
+                            Y, (int)N, (int)M, (int)K, static_cast<const float *>(rs32),
+                            dev_status));
 }

@@ -175,12 +175,33 @@ rfp2_status rfp2_moe_gemv(const uint8_t *W, int64_t E, int64_t M, int64_t K,
  *   W  uint8 [M, K/32, 10] device.  X bf16 bits [N, K] device, 16-byte
  *   aligned.  Y fp32 [N, M] device (output), 16-byte aligned.
  *   M % 16 == 0, N >= 1, K % 256 == 0.
- *   workspace: rfp2_gemm_workspace_bytes(M, K) bytes, 1024-byte aligned
+ *   workspace: rfp2_gemm_workspace_bytes(M, K) bytes, 256-byte aligned
  *   (holds the expanded bf16 weights [M, K]).
  * Errors: EINVAL, ESHAPE, EUNSUPPORTED, EALIGN, EWORKSPACE, ECUDA.
  */
 size_t rfp2_gemm_workspace_bytes(int64_t M, int64_t K);
 rfp2_status rfp2_gemm(const uint8_t *W, int64_t M, int64_t K, const uint16_t *X, int64_t N,
+                      float *Y, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                      rfp2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * HFP4G32 prefill GEMM: Y[n, m] = row_scale_a(m) * sum_k E2M1[c_mk] *
+ * 2^(e_mk - 127) * X[n, k] ("HFP4", sections "Element format (OCP E2M1)",
+ * "Block scale - UE8M0", "Per-row second-level scale (FP16)" and "Byte
+ * layout - HFP4G32"; no activation quantization on this path).  The weights
+ * are expanded exactly to bf16 in the workspace (an E2M1 value times a power
+ * of two has at most two significant bits; block byte 0xFF gives NaN), the
+ * product runs on the tensor cores with fp32 accumulation, and the f16 row
+ * scale multiplies each output in fp32.
+ *   W uint8 [M, 16 + 17*K/32] device (HFP4G32 rows), 16-byte aligned;
+ *   X bf16 bit patterns [N, K] device, 16-byte aligned; Y fp32 [N, M] device,
+ *   16-byte aligned; workspace device, hfp4_gemm_workspace_bytes(M, K) bytes,
+ *   256-byte aligned (bf16 weights [M, K], then the row scales as fp32).
+ * Errors: EINVAL, ESHAPE, EUNSUPPORTED (K % 256, M % 16), EWORKSPACE, EALIGN,
+ * ECUDA; a bounded device wait that ran out stores ETIMEOUT in dev_status.
+ */
+size_t hfp4_gemm_workspace_bytes(int64_t M, int64_t K);
+rfp2_status hfp4_gemm(const uint8_t *W, int64_t M, int64_t K, const uint16_t *X, int64_t N,
                       float *Y, void *workspace, size_t workspace_bytes, int32_t *dev_status,
                       rfp2_stream_t stream);
 

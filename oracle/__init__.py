@@ -281,6 +281,16 @@ def hfp4_gemv(P: np.ndarray, M: int, K: int, x: np.ndarray, rows=None) -> np.nda
     return y
 
 
+def hfp4_gemm(P: np.ndarray, M: int, K: int, X_bf16: np.ndarray, rows=None) -> np.ndarray:
+    """Prefill: fp64 Y [N, len(rows)] = sum_k w[m, k] * X[n, k] for bf16 tokens
+    X (given as 16-bit patterns): the GEMV loop formula of hfp4_gemv over every
+    token, each bf16 value widened exactly to fp32 (no activation
+    quantization on this path)."""
+    X = np.ascontiguousarray(np.atleast_2d(X_bf16)).view(np.uint16)
+    x = (X.astype(np.uint32) << 16).view(np.float32)
+    return hfp4_gemv(P, M, K, x, rows)
+
+
 def f32_to_f16_bits(v: float) -> int:
     return int(_load().orc_f32_to_f16_bits(float(v)))
 

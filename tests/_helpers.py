@@ -52,6 +52,34 @@ def decode_weights_independent(P: np.ndarray, M: int, K: int) -> np.ndarray:
     return levels[unpack_codes(P, M, K)] * s
 
 
+# OCP MX v1.0 E2M1 magnitudes by the low three code bits (bit 3 is the sign).
+E2M1_OCP = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def decode_hfp4_independent(P: np.ndarray, M: int, K: int, row_scale: bool = True) -> np.ndarray:
+    """float64 [M, K] from HFP4G32 rows, with numpy alone: row_scale_a as the
+    little-endian f16 in bytes 0-1, then per 17-byte block the UE8M0 byte
+    (2^(e-127), 0xFF -> NaN) and 16 code bytes, the low nibble the even
+    element.  row_scale=False leaves out row_scale_a."""
+    P = np.asarray(P, np.uint8).reshape(M, -1)
+    nb = K // 32
+    rs = P[:, 0:2].copy().view("<f2").astype(np.float64).reshape(M)
+    blocks = P[:, 16:16 + 17 * nb].reshape(M, nb, 17)
+    e = blocks[:, :, 0].astype(np.int64)
+    scale = np.where(e == 255, np.nan, np.ldexp(1.0, e - 127))
+    codes = blocks[:, :, 1:]
+    c = np.stack([codes & 15, codes >> 4], axis=-1).reshape(M, nb, 32)
+    val = np.where(c & 8, -1.0, 1.0) * E2M1_OCP[c & 7] * scale[:, :, None]
+    if row_scale:
+        val = val * rs[:, None, None]
+    return val.reshape(M, K)
+
+
+def bf16_bits_to_f64(X: np.ndarray) -> np.ndarray:
+    X = np.ascontiguousarray(X).view(np.uint16)
+    return (X.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
 def rel_err_rows(y, ref) -> np.ndarray:
     """Normwise relative error per row: ||y - ref||_2 / ||ref||_2."""
     y = np.asarray(y, np.float64)

@@ -13,8 +13,8 @@ import numpy as np
 import pytest
 
 import oracle
-from synth import hfp4_gemv
-from _helpers import load_golden, rel_err_rows
+from synth import child_rngs, float32_to_bf16_bits, hfp4_gemv, normal_weights
+from _helpers import bf16_bits_to_f64, decode_hfp4_independent, load_golden, rel_err_rows
 
 
 def _mags():
@@ -174,3 +174,40 @@ def test_gemv_loop_formula_matches_decoded_dot():
     np.testing.assert_array_equal(oracle.hfp4_gemv(P, 40, 1024, w["x"], rows=rows), y[:, rows])
     # decoded weights approximate W within the format's error (sanity, not a pin)
     assert np.all(rel_err_rows(ref, w["x"].astype(np.float64) @ w["W"].T.astype(np.float64)) < 0.2)
+
+
+def test_decode_matches_independent_decoder():
+    w = hfp4_gemv(M=24, K=512, N=1)
+    P = oracle.hfp4_pack(w["W"])
+    P[3, 16 + 17 * 2] = 0xFF   # a NaN block
+    P[5, 16] = 0x00            # the subnormal block scale 2^-127
+    np.testing.assert_array_equal(oracle.hfp4_decode(P, 24, 512), decode_hfp4_independent(P, 24, 512))
+
+
+def test_gemm_matches_independent_decoded_product():
+    """Prefill: Y = X W^T over bf16 tokens (no activation quantization), against
+    numpy's product of the independently decoded weights in fp64."""
+    r_w, r_x = child_rngs(21, 2)
+    M, K, N = 36, 768, 5
+    P = oracle.hfp4_pack(normal_weights(r_w, M, K, 0.03))
+    X = float32_to_bf16_bits(r_x.standard_normal((N, K)).astype(np.float32))
+    Y = oracle.hfp4_gemm(P, M, K, X)
+    ref = bf16_bits_to_f64(X) @ decode_hfp4_independent(P, M, K).T
+    assert np.all(rel_err_rows(Y, ref) <= 1e-12)
+    rows = np.array([35, 0, 17])
+    np.testing.assert_array_equal(oracle.hfp4_gemm(P, M, K, X, rows=rows), Y[:, rows])
+
+
+def test_gemm_exact_when_every_weight_is_on_the_lattice():
+    """Rows holding 6 have row_scale_a = 1 and every value of {+-6, +-3, +-1.5,
+    +-1, 0} on its block lattice, so the packing is exact and, with small
+    integer tokens, so is every output."""
+    rng = np.random.default_rng(5)
+    M, K, N = 8, 256, 3
+    W = rng.choice(np.array([-6.0, -3.0, -1.5, -1.0, 0.0, 1.0, 1.5, 3.0, 6.0]), (M, K))
+    W[:, 0] = 6.0
+    P = oracle.hfp4_pack(W.astype(np.float32))
+    np.testing.assert_array_equal(oracle.hfp4_decode(P, M, K), W)
+    Xf = rng.integers(-8, 9, (N, K)).astype(np.float32)
+    Y = oracle.hfp4_gemm(P, M, K, float32_to_bf16_bits(Xf))
+    np.testing.assert_array_equal(Y, Xf.astype(np.float64) @ W.T)
