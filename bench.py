@@ -368,15 +368,9 @@ def _graph_us(torch, fn, calls, reps):
     return ms * 1e3
 
 
-def secondary(torch, gl, peaks):
-    """The other rows of the hot path, each on its own synthetic workload, in
-    CUDA graphs of back-to-back calls over weight copies larger than L2."""
-    import numpy as np
-    from synth import hfp4_gemv, moe_expert_weights, moe_gemv, prefill_gemm
-    out = {}
-    hbm = peaks["hbm_gbs"]
-
-    # MoE bulk-expert GEMV: 256 experts of 768 x 2048, 16 tokens, top-8
+def _sec_moe(torch, gl, peaks, reps=3):
+    """MoE bulk-expert GEMV: 256 experts of 768 x 2048, 16 tokens, top-8."""
+    from synth import moe_expert_weights, moe_gemv
     E, M, K, T, top_k = 256, 768, 2048, 16, 8
     w = moe_gemv(E=E, M=M, K=K, T=T, top_k=top_k, seed=2, experts=False)
     copies = 3
@@ -392,16 +386,21 @@ def secondary(torch, gl, peaks):
     touched = len(set(w["ids"].ravel().tolist()))
     nbytes = touched * M * K // 32 * 10
     us = _graph_us(torch, lambda i: gl.rfp2_moe_gemv(Pc[i % copies], E, M, K, ids, x, y=y,
-                                                     workspace=ws), 200, 3)
-    out["moe_gemv"] = {
+                                                     workspace=ws), 200, reps)
+    del Pc, ids, x, y, ws
+    torch.cuda.empty_cache()
+    return {"moe_gemv": {
         "workload": f"256 experts x ROCmFP2 [768, 2048], 16 tokens, top-8 ({touched} experts "
                     f"touched), seed 2; {copies} copies of all experts rotate",
         "value": round(nbytes / us / 1e3, 1), "unit": "GB/s (touched experts' packed bytes)",
         "us_per_call": round(us, 2), "bytes_per_call": nbytes,
-        "frac_of_hbm_peak": round(nbytes / us / 1e3 / hbm, 4)}
-    del Pc, ids, x, y, ws
+        "frac_of_hbm_peak": round(nbytes / us / 1e3 / peaks["hbm_gbs"], 4)}}
 
-    # HFP4G32 GEMV 8192 x 8192, batch 1 and 8
+
+def _sec_hfp4(torch, gl, peaks, reps=3):
+    """HFP4G32 GEMV 8192 x 8192, batch 1 and 8."""
+    from synth import hfp4_gemv
+    out = {}
     w = hfp4_gemv(N=8)
     M, K = w["W"].shape
     P = gl.hfp4_pack_weights(torch.from_numpy(w["W"]).cuda())
@@ -413,52 +412,76 @@ def secondary(torch, gl, peaks):
         y = torch.empty((N, M), dtype=torch.float32, device="cuda")
         ws = torch.empty(gl.hfp4_gemv_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
         us = _graph_us(torch, lambda i: gl.hfp4_gemv(Pc[i % copies], M, K, x, y=y, workspace=ws),
-                       200, 3)
+                       200, reps)
         out[f"hfp4_gemv_batch{N}"] = {
             "workload": f"HFP4G32 [8192, 8192] N(0, 0.02^2) seed 4, batch {N}; {copies} copies rotate",
             "value": round(P.numel() / us / 1e3, 1), "unit": "GB/s (packed bytes)",
             "us_per_call": round(us, 2), "bytes_per_call": int(P.numel()),
-            "frac_of_hbm_peak": round(P.numel() / us / 1e3 / hbm, 4)}
+            "frac_of_hbm_peak": round(P.numel() / us / 1e3 / peaks["hbm_gbs"], 4)}
     del P, Pc
     torch.cuda.empty_cache()
+    return out
 
-    # prefill GEMM 17408 x 5120 x 2048 tokens (expansion to bf16 included)
+
+def _sec_gemm(torch, gl, peaks, hfp4=False, reps=3):
+    """Prefill GEMM 17408 x 5120 x 2048 tokens (expansion to bf16 included),
+    ROCmFP2 or (hfp4=True) HFP4G32 weights."""
+    import numpy as np
+    from synth import prefill_gemm
     w = prefill_gemm()
     M, K = w["W"].shape
     N = w["X"].shape[0]
-    P = gl.rfp2_pack_weights(torch.from_numpy(w["W"]).cuda())
+    Wd = torch.from_numpy(w["W"]).cuda()
+    P = gl.hfp4_pack_weights(Wd) if hfp4 else gl.rfp2_pack_weights(Wd)
+    del Wd
     X = torch.from_numpy(w["X"].view(np.int16)).cuda()
     Y = torch.empty((N, M), dtype=torch.float32, device="cuda")
-    ws = torch.empty(gl.rfp2_gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
-    us = _graph_us(torch, lambda i: gl.rfp2_gemm(P, M, K, X, Y=Y, workspace=ws), 20, 3)
+    if hfp4:
+        ws = torch.empty(gl.hfp4_gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+        fn = lambda i: gl.hfp4_gemm(P, M, K, X, Y=Y, workspace=ws)
+    else:
+        ws = torch.empty(gl.rfp2_gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+        fn = lambda i: gl.rfp2_gemm(P, M, K, X, Y=Y, workspace=ws)
+    us = _graph_us(torch, fn, 20, reps)
     tflops = 2.0 * M * K * N / us / 1e6
-    out["prefill_gemm"] = {
-        "workload": "ROCmFP2 [17408, 5120] N(0, 0.015^2) x bf16 [2048, 5120] (0.5% x20), seed 3",
+    fmt = "HFP4G32" if hfp4 else "ROCmFP2"
+    del P, X, Y, ws
+    torch.cuda.empty_cache()
+    return {("hfp4_prefill_gemm" if hfp4 else "prefill_gemm"): {
+        "workload": f"{fmt} [17408, 5120] N(0, 0.015^2) x bf16 [2048, 5120] (0.5% x20), seed 3",
         "value": round(tflops, 1), "unit": "TFLOP/s (2*M*N*K, expansion included)",
         "us_per_call": round(us, 1),
         "frac_of_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),
         "frac_of_bf16_sustained": round(tflops / peaks["bf16_tflops_sustained"], 4),
-        "bound": "tensor", "peak_source": peaks["source"] + " bf16_tflops (cuBLAS bf16)"}
-    del P, X, Y, ws
-    torch.cuda.empty_cache()
+        "bound": "tensor", "peak_source": peaks["source"] + " bf16_tflops (cuBLAS bf16)"}}
 
-    # HFP4G32 prefill GEMM on the same shapes (expansion to bf16 included)
-    P = gl.hfp4_pack_weights(torch.from_numpy(w["W"]).cuda())
-    X = torch.from_numpy(w["X"].view(np.int16)).cuda()
-    Y = torch.empty((N, M), dtype=torch.float32, device="cuda")
-    ws = torch.empty(gl.hfp4_gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
-    us = _graph_us(torch, lambda i: gl.hfp4_gemm(P, M, K, X, Y=Y, workspace=ws), 20, 3)
-    tflops = 2.0 * M * K * N / us / 1e6
-    out["hfp4_prefill_gemm"] = {
-        "workload": "HFP4G32 [17408, 5120] N(0, 0.015^2) x bf16 [2048, 5120] (0.5% x20), seed 3",
-        "value": round(tflops, 1), "unit": "TFLOP/s (2*M*N*K, expansion included)",
-        "us_per_call": round(us, 1),
-        "frac_of_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),
-        "frac_of_bf16_sustained": round(tflops / peaks["bf16_tflops_sustained"], 4),
-        "bound": "tensor", "peak_source": peaks["source"] + " bf16_tflops (cuBLAS bf16)"}
-    del P, X, Y, ws
-    torch.cuda.empty_cache()
+
+SECONDARY_ROWS = {
+    "moe": _sec_moe,
+    "hfp4": _sec_hfp4,
+    "gemm": lambda torch, gl, peaks, reps=3: _sec_gemm(torch, gl, peaks, False, reps),
+    "hgemm": lambda torch, gl, peaks, reps=3: _sec_gemm(torch, gl, peaks, True, reps),
+}
+
+
+def secondary(torch, gl, peaks):
+    """The other rows of the hot path, each on its own synthetic workload, in
+    CUDA graphs of back-to-back calls over weight copies larger than L2."""
+    out = {}
+    for fn in SECONDARY_ROWS.values():
+        out.update(fn(torch, gl, peaks))
     return out
+
+
+def run_only(args):
+    """One secondary row alone (one graph replay), for profiler captures."""
+    import torch
+    import gemm_rocmfp2_mul_gb300 as gl
+    torch.cuda.set_device(0)
+    gl.build()
+    gl.lib()
+    out = SECONDARY_ROWS[args.only](torch, gl, load_peaks(), reps=1)
+    print(json.dumps(out), flush=True)
 
 
 def run_e2e(torch, gl, w, Pc, copies, steps):
@@ -579,9 +602,13 @@ def main():
                     help="time budget of the reference arm's K + W steps")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per GEMV launch from an ncu capture of this kernel")
+    ap.add_argument("--only", choices=sorted(SECONDARY_ROWS),
+                    help="time one secondary row alone (for profiler captures) and exit")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_gpu(args)
 

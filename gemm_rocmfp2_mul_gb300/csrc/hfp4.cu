@@ -26,6 +26,7 @@
 //    combined in shared memory.  All waits are bounded.
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -57,19 +58,29 @@ __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
     return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
 
-// One CTA per activation column: power-of-two scaling and the two-piece f16
-// split, written in the B-fragment order of mma.m16n8k16 for the K
-// permutation used by the GEMV (MMA k 2p+i <-> element 8p+4s+i and
-// 2p+8+i <-> 8p+4s+2+i of a 32-element block, k-step s of the block).
+// Grid (slices, N): every CTA of column n finds max |x| over the whole column
+// (the column is a few KB and read from L2 by each slice), then writes its
+// slice of the power-of-two-scaled two-piece f16 split, in the B-fragment
+// order of mma.m16n8k16 for the K permutation used by the GEMV (MMA k 2p+i
+// <-> element 8p+4s+i and 2p+8+i <-> 8p+4s+2+i of a 32-element block, k-step
+// s of the block).
 __global__ void __launch_bounds__(256) hfp4_split_kernel(const float *__restrict__ x, int N, int K,
                                                          int *kc_out, uint4 *frag) {
     __shared__ float wmax[8];
     pdl_wait();
     pdl_launch_dependents();
-    const int n = blockIdx.x;
+    const int n = blockIdx.y;
     const float *xr = x + (int64_t)n * K;
     float amax = 0.0f;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) amax = fmaxf(amax, fabsf(xr[k]));
+    if ((reinterpret_cast<uintptr_t>(xr) & 15) == 0) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(xr);
+        for (int k = threadIdx.x; k < K / 4; k += blockDim.x) {
+            const float4 v = __ldg(x4 + k);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+    } else {
+        for (int k = threadIdx.x; k < K; k += blockDim.x) amax = fmaxf(amax, fabsf(__ldg(xr + k)));
+    }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -78,9 +89,11 @@ __global__ void __launch_bounds__(256) hfp4_split_kernel(const float *__restrict
     amax = 0.0f;
     for (int i = 0; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, wmax[i]);
     const int kc = amax > 0.0f ? ilogbf(amax) : 0;  // max |x| * 2^-kc in [1, 2)
-    if (threadIdx.x == 0) kc_out[n] = kc;
+    if (threadIdx.x == 0 && blockIdx.x == 0) kc_out[n] = kc;
     const int entries = (K / 16) * 4;
-    for (int e = threadIdx.x; e < entries; e += blockDim.x) {
+    const int per = (entries + gridDim.x - 1) / gridDim.x;
+    const int e0 = blockIdx.x * per, e1 = min(entries, e0 + per);
+    for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
         const int ks = e >> 2, p = e & 3;
         const int base = (ks >> 1) * 32 + 8 * p + 4 * (ks & 1);
         __half h1[4], h2[4];
@@ -379,8 +392,10 @@ extern "C" rfp2_status hfp4_gemv(const uint8_t *W, int64_t M, int64_t K, const f
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int *kc = static_cast<int *>(workspace);
     uint4 *frag = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(workspace) + 256);
-    cudaError_t e = launch(hfp4_split_kernel, dim3((unsigned)N), dim3(256), 0, s, true, x, (int)N,
-                           (int)K, kc, frag);
+    // slices of K per column: about 1024 fragment entries (4096 elements) each
+    const int slices = (int)std::min<int64_t>(64, std::max<int64_t>(1, K / 4096));
+    cudaError_t e = launch(hfp4_split_kernel, dim3((unsigned)slices, (unsigned)N), dim3(256), 0, s,
+                           true, x, (int)N, (int)K, kc, frag);
     if (e != cudaSuccess) return RFP2_ECUDA;
     // stages: as many 64-row x 1024-K tiles (plus their fragments) as fit
     const size_t per_stage = kWStageBytes + (size_t)64 * N * 64;
