@@ -456,7 +456,37 @@ def _sec_gemm(torch, gl, peaks, hfp4=False, reps=3):
         "bound": "tensor", "peak_source": peaks["source"] + " bf16_tflops (cuBLAS bf16)"}}
 
 
+def _sec_verify(torch, gl, peaks, reps=3):
+    """Verify batches of 32 and 128 tokens on the decode weights (tensor-core
+    GEMV on Q8_1 activations, weights expanded once per call)."""
+    from synth import decode_gemv
+    out = {}
+    w = decode_gemv(N=1)
+    M, K = w["W"].shape
+    P = gl.rfp2_pack_weights(torch.from_numpy(w["W"]).cuda())
+    copies = 8
+    Pc = torch.empty((copies,) + tuple(P.shape), dtype=torch.uint8, device="cuda")
+    Pc[:] = P
+    for N in (32, 128):
+        x = torch.from_numpy(np.random.default_rng(N).standard_normal((N, K)).astype(np.float32)).cuda()
+        y = torch.empty((N, M), dtype=torch.float32, device="cuda")
+        ws = torch.empty(gl.rfp2_gemv_batched_workspace_bytes(M, K, N), dtype=torch.uint8,
+                         device="cuda")
+        us = _graph_us(torch, lambda i: gl.rfp2_gemv_batched(Pc[i % copies], M, K, x, y=y,
+                                                             workspace=ws), 50, reps)
+        out[f"verify_batch{N}"] = {
+            "workload": f"ROCmFP2 decode weights [14336, 4096] (seed 1), {N} tokens N(0,1); "
+                        f"{copies} copies rotate",
+            "value": round(P.numel() / us / 1e3, 1), "unit": "GB/s (packed bytes)",
+            "tflops": round(2.0 * M * K * N / us / 1e6, 1),
+            "us_per_call": round(us, 2), "bytes_per_call": int(P.numel())}
+    del P, Pc
+    torch.cuda.empty_cache()
+    return out
+
+
 SECONDARY_ROWS = {
+    "verify": _sec_verify,
     "moe": _sec_moe,
     "hfp4": _sec_hfp4,
     "gemm": lambda torch, gl, peaks, reps=3: _sec_gemm(torch, gl, peaks, False, reps),

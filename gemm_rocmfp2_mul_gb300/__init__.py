@@ -62,6 +62,8 @@ _SIGNATURES = {
     "rfp2_moe_gemv": (_I32, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _P, _SZ, _P, _P]),
     "rfp2_gemm_workspace_bytes": (_SZ, [_I64, _I64]),
     "rfp2_gemm": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
+    "rfp2_gemv_batched_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
+    "rfp2_gemv_batched": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
     "hfp4_gemm_workspace_bytes": (_SZ, [_I64, _I64]),
     "hfp4_gemm": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
     "hfp4_gemv_workspace_bytes": (_SZ, [_I64, _I64]),
@@ -248,6 +250,24 @@ def rfp2_gemm(W, M, K, X, Y=None, workspace=None, dev_status=None):
     _check(lib().rfp2_gemm(_ptr(W), M, K, _ptr(X), N, _ptr(Y), _ptr(ws), ws.numel(),
                            _ptr(dev_status), _stream()), "rfp2_gemm")
     return Y
+
+
+def rfp2_gemv_batched_workspace_bytes(M: int, K: int, N: int) -> int:
+    return int(lib().rfp2_gemv_batched_workspace_bytes(M, K, N))
+
+
+def rfp2_gemv_batched(W, M, K, x, y=None, workspace=None, dev_status=None):
+    """ROCmFP2 GEMV on Q8_1 activations for verify batches (tensor cores):
+    y fp32 [N, M] from fp32 x [N, K]."""
+    torch = _torch()
+    _need(W, torch.uint8, "W")
+    _need(x, torch.float32, "x")
+    N = x.shape[0]
+    y = _empty((N, M), torch.float32, x) if y is None else _need(y, torch.float32, "y")
+    ws = _workspace(workspace, rfp2_gemv_batched_workspace_bytes(M, K, N), x)
+    _check(lib().rfp2_gemv_batched(_ptr(W), M, K, _ptr(x), N, _ptr(y), _ptr(ws), ws.numel(),
+                                   _ptr(dev_status), _stream()), "rfp2_gemv_batched")
+    return y
 
 
 def hfp4_gemm_workspace_bytes(M: int, K: int) -> int:

@@ -21,9 +21,11 @@
 //     store fp32 rows.  Every wait is bounded; tensor memory is always freed.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
+#include "expand.cuh"
 #include "rfp2_decode.cuh"
 #include "tcgen05.cuh"
 #include "tma.cuh"
@@ -44,35 +46,6 @@ constexpr uint32_t kTmemCols = 256;
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
 
 // ---- expand ----------------------------------------------------------------
-__global__ void __launch_bounds__(256) expand_bf16_kernel(const uint8_t *__restrict__ W,
-                                                          int64_t nblocks,
-                                                          __nv_bfloat16 *__restrict__ out) {
-    pdl_wait();
-    pdl_launch_dependents();
-    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (j >= nblocks) return;
-    const uint8_t *b = W + j * 10;
-    uint32_t lo = b[0] | (b[1] << 8) | (b[2] << 16) | ((uint32_t)b[3] << 24);
-    uint32_t hi = b[4] | (b[5] << 8) | (b[6] << 16) | ((uint32_t)b[7] << 24);
-    float s0, s1;
-    decode_scale_pair((uint32_t)b[8] | ((uint32_t)b[9] << 8), s0, s1);
-    const float lv[4] = {-4.0f, -1.0f, 1.0f, 4.0f};
-    uint4 *o = reinterpret_cast<uint4 *>(out + j * 32);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {  // 8 weights per 16-byte store
-        const uint32_t c = q < 2 ? lo >> (16 * q) : hi >> (16 * (q - 2));
-        const float s = q < 2 ? s0 : s1;
-        uint32_t v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat16 w0 = __float2bfloat16_rn(lv[(c >> (4 * i)) & 3] * s);
-            const __nv_bfloat16 w1 = __float2bfloat16_rn(lv[(c >> (4 * i + 2)) & 3] * s);
-            v[i] = (uint32_t)__bfloat16_as_ushort(w0) | ((uint32_t)__bfloat16_as_ushort(w1) << 16);
-        }
-        o[q] = make_uint4(v[0], v[1], v[2], v[3]);
-    }
-}
-
 // HFP4G32 rows -> bf16: element = E2M1[c] * 2^(e-127) (at most two
 // significant bits times a power of two: exact in bf16, including the
 // subnormal range; block byte 0xFF gives NaN), and the row scale row_scale_a
@@ -125,10 +98,11 @@ __global__ void __launch_bounds__(256) hfp4_expand_bf16_kernel(const uint8_t *__
 }
 
 // ---- GEMM --------------------------------------------------------------------
+// colscale[m]: optional per-weight-row factor applied to every output.
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_bf16_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-                     float *__restrict__ Y, int Ntok, int Mw, int K, const float *__restrict__ colscale,
-                     int32_t *status) {
+    gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+                float *__restrict__ Y, int Ntok, int Mw, int K, const float *__restrict__ colscale,
+                int32_t *status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -269,7 +243,7 @@ extern "C" rfp2_status rfp2_gemm(const uint8_t *W, int64_t M, int64_t K, const u
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     __nv_bfloat16 *wexp = static_cast<__nv_bfloat16 *>(workspace);
     const int64_t nblocks = M * (K / 32);
-    cudaError_t e = launch(expand_bf16_kernel, dim3((unsigned)((nblocks + 255) / 256)), dim3(256),
+    cudaError_t e = launch(expand_kernel<__nv_bfloat16>, dim3((unsigned)((nblocks + 255) / 256)), dim3(256),
                            0, s, true, W, nblocks, wexp);
     if (e != cudaSuccess) return RFP2_ECUDA;
     CUtensorMap xmap, wmap;
@@ -284,13 +258,13 @@ extern "C" rfp2_status rfp2_gemm(const uint8_t *W, int64_t M, int64_t K, const u
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 64 && !configured[dev]) {
-            if (set_smem_limit(gemm_bf16_kernel, (int)kSmemBytes) != cudaSuccess) return RFP2_ECUDA;
+            if (set_smem_limit(gemm_kernel, (int)kSmemBytes) != cudaSuccess) return RFP2_ECUDA;
             configured[dev] = 1;
         }
     }
     const dim3 grid((unsigned)((N + BM - 1) / BM), (unsigned)((M + BN - 1) / BN));
-    return from_cuda(launch(gemm_bf16_kernel, grid, dim3(kThreads), kSmemBytes, s, true, xmap, wmap,
-                            Y, (int)N, (int)M, (int)K, static_cast<const float *>(nullptr),
+    return from_cuda(launch(gemm_kernel, grid, dim3(kThreads), kSmemBytes, s, true, xmap, wmap, Y,
+                            (int)N, (int)M, (int)K, static_cast<const float *>(nullptr),
                             dev_status));
 }
 
@@ -337,12 +311,12 @@ extern "C" rfp2_status hfp4_gemm(const uint8_t *W, int64_t M, int64_t K, const u
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 64 && !configured[dev]) {
-            if (set_smem_limit(gemm_bf16_kernel, (int)kSmemBytes) != cudaSuccess) return RFP2_ECUDA;
+            if (set_smem_limit(gemm_kernel, (int)kSmemBytes) != cudaSuccess) return RFP2_ECUDA;
             configured[dev] = 1;
         }
     }
     const dim3 grid((unsigned)((N + BM - 1) / BM), (unsigned)((M + BN - 1) / BN));
-    return from_cuda(launch(gemm_bf16_kernel, grid, dim3(kThreads), kSmemBytes, s, true, xmap, wmap,
-                            Y, (int)N, (int)M, (int)K, static_cast<const float *>(rs32),
+    return from_cuda(launch(gemm_kernel, grid, dim3(kThreads), kSmemBytes, s, true, xmap, wmap, Y,
+                            (int)N, (int)M, (int)K, static_cast<const float *>(rs32),
                             dev_status));
 }

@@ -54,6 +54,11 @@ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with A and B f16 (format field 0).
+constexpr uint32_t idesc_f16_f32(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 RFP2_DEV void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                         uint32_t accumulate) {

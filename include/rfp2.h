@@ -185,6 +185,28 @@ rfp2_status rfp2_gemm(const uint8_t *W, int64_t M, int64_t K, const uint16_t *X,
                       rfp2_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * ROCmFP2 GEMV for verify batches (tens to hundreds of tokens): the result of
+ * rfp2_gemv (Q8_1-style activations, "ROCmFP2 codebook research report",
+ * section "03 Runtime": expand each block once and reuse it for every
+ * activation column) computed on the tensor cores.  The weights are expanded
+ * exactly to f16, each token's quantized activations q * dA are scaled by a
+ * power of two and split into two f16 pieces (relative residual <= 2^-22),
+ * and both pieces are multiplied with fp32 accumulation; each output is
+ * within about 1e-6 relative of the exact int-path result.
+ *   x fp32 [N, K] device, 1 <= N <= 65535; y fp32 [N, M] device, 16-byte
+ *   aligned; W 16-byte aligned; workspace device,
+ *   rfp2_gemv_batched_workspace_bytes(M, K, N) bytes, 256-byte aligned
+ *   (f16 weights [M, K], then q int8 [N, K], then d fp32 [N, K/32], each at
+ *   a 256-byte boundary, then the activation pieces).
+ * Errors: EINVAL, ESHAPE, EUNSUPPORTED (K % 256, M % 16), EWORKSPACE, EALIGN,
+ * ECUDA; a bounded device wait that ran out stores ETIMEOUT in dev_status.
+ */
+size_t rfp2_gemv_batched_workspace_bytes(int64_t M, int64_t K, int64_t N);
+rfp2_status rfp2_gemv_batched(const uint8_t *W, int64_t M, int64_t K, const float *x,
+                              int64_t N, float *y, void *workspace, size_t workspace_bytes,
+                              int32_t *dev_status, rfp2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * HFP4G32 prefill GEMM: Y[n, m] = row_scale_a(m) * sum_k E2M1[c_mk] *
  * 2^(e_mk - 127) * X[n, k] ("HFP4", sections "Element format (OCP E2M1)",
  * "Block scale - UE8M0", "Per-row second-level scale (FP16)" and "Byte
