@@ -46,6 +46,14 @@ constexpr uint32_t kTmemCols = 256;
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
 
 // ---- expand ----------------------------------------------------------------
+// OCP E2M1 code -> float: magnitude index k = c & 7 is 0 (0), 1 (0.5) or,
+// for k >= 2, 2^((k >> 1) - 1) * (1 + (k & 1) / 2); bit 3 is the sign.
+__device__ __forceinline__ float e2m1_float(uint32_t c) {
+    const uint32_t k = c & 7;
+    const uint32_t mag = k >= 2 ? ((((k >> 1) + 126) << 23) | ((k & 1) << 22)) : (k ? 0x3F000000u : 0u);
+    return __uint_as_float(mag | ((c & 8) << 28));
+}
+
 // HFP4G32 rows -> bf16: element = E2M1[c] * 2^(e-127) (at most two
 // significant bits times a power of two: exact in bf16, including the
 // subnormal range; block byte 0xFF gives NaN), and the row scale row_scale_a
@@ -78,7 +86,6 @@ __global__ void __launch_bounds__(256) hfp4_expand_bf16_kernel(const uint8_t *__
     u[4] = v[4] >> sh;
     const uint32_t e = u[0] & 0xFFu;
     const float sc = __uint_as_float(e == 0 ? 0x00400000u : e == 0xFF ? 0x7FC00000u : e << 23);
-    const float mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
     uint4 *o = reinterpret_cast<uint4 *>(out + j * 32);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {  // 8 weights (code bytes 1+4q .. 4+4q) per 16-byte store
@@ -87,9 +94,8 @@ __global__ void __launch_bounds__(256) hfp4_expand_bf16_kernel(const uint8_t *__
         for (int i = 0; i < 4; ++i) {
             const int t = 1 + 4 * q + i;  // byte of the block
             const uint32_t byte = (u[t >> 2] >> (8 * (t & 3))) & 0xFFu;
-            const uint32_t c0 = byte & 15, c1 = byte >> 4;
-            const float f0 = (c0 & 8 ? -mag[c0 & 7] : mag[c0 & 7]) * sc;
-            const float f1 = (c1 & 8 ? -mag[c1 & 7] : mag[c1 & 7]) * sc;
+            const float f0 = e2m1_float(byte & 15) * sc;
+            const float f1 = e2m1_float(byte >> 4) * sc;
             w[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f0)) |
                    ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f1)) << 16);
         }

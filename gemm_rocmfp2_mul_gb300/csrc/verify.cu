@@ -12,12 +12,12 @@
 //  3. split: x^ = q * dA scaled by 2^-kc (per token) into two f16 pieces,
 //     hi + lo, relative residual <= 2^-22;
 //  4. vb_gemm: one CTA per 128 weight rows x BNT tokens.  Warp 0 streams
-//     K-major 64-element slices of the weights and of one activation piece
+//     K-major 64-element slices of the weights and of both activation pieces
 //     with 2-D TMA (SWIZZLE_128B) into a ring; one thread of warp 1 issues
 //     tcgen05.mma kind::f16 (M = 128 weight rows, N = BNT tokens, K = 16,
 //     f16 in, fp32 in tensor memory).  The tensor cores' fp32 accumulation
 //     does not round to nearest, which over 2K/16 steps would cost ~1.5e-5
-//     relative; so the product is accumulated in short chunks (4 k-slices)
+//     relative; so the product is accumulated in short chunks (16 MMAs)
 //     in two alternating tensor-memory buffers, and warps 2-5 add each
 //     finished chunk into fp32 registers (one weight row per thread, BNT
 //     token sums) while the next chunk runs.  They then store y with 2^kc.
@@ -36,13 +36,14 @@ namespace {
 constexpr int VBM = 128;      // weight rows per tile (UMMA M)
 constexpr int VBK = 64;       // K per stage: one 128-byte swizzle row of f16
 constexpr int VUK = 16;       // K per UMMA instruction
-constexpr int VSTAGES = 6;
-constexpr int VCHUNK = 4;     // k-slices per tensor-memory accumulation chunk
+constexpr int VSTAGES = 4;
+constexpr int VCHUNK = 2;     // stages (2 x 8 MMAs) per tensor-memory accumulation chunk
 constexpr int VTHREADS = 6 * 32;
 constexpr int kABytes = VBM * VBK * 2;
 
+// one stage: the weight slice and both activation pieces of the same K range
 template <int BNT>
-constexpr int stage_bytes() { return kABytes + BNT * VBK * 2; }
+constexpr int stage_bytes() { return kABytes + 2 * BNT * VBK * 2; }
 template <int BNT>
 constexpr size_t vb_smem_bytes() { return 1024 + (size_t)VSTAGES * stage_bytes<BNT>() + 256; }
 
@@ -103,8 +104,9 @@ __global__ void __launch_bounds__(VTHREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile_m = blockIdx.x, tile_n = blockIdx.y;
     const int nk = K / VBK;
-    const int nt = 2 * nk;  // both pieces
+    const int nt = nk;
     const int nchunks = (nt + VCHUNK - 1) / VCHUNK;
+    constexpr int kBBytes = BNT * VBK * 2;
 
     if (threadIdx.x == 0) {
         prefetch_tensor_map(&wmap);
@@ -143,10 +145,10 @@ __global__ void __launch_bounds__(VTHREADS, 1)
             }
             if (*abort_flag) break;
             uint8_t *a = smem + (size_t)s * SB;
-            const int piece = t / nk, kk = t - piece * nk;
             mbar_arrive_expect_tx(&full[s], SB);
-            tma_load_2d(a, &wmap, kk * VBK, tile_m * VBM, &full[s]);
-            tma_load_2d(a + kABytes, piece ? &lmap : &hmap, kk * VBK, tile_n * BNT, &full[s]);
+            tma_load_2d(a, &wmap, t * VBK, tile_m * VBM, &full[s]);
+            tma_load_2d(a + kABytes, &hmap, t * VBK, tile_n * BNT, &full[s]);
+            tma_load_2d(a + kABytes + kBBytes, &lmap, t * VBK, tile_n * BNT, &full[s]);
         }
         for (int i = max(0, t - VSTAGES); i < t; ++i)
             if (!mbar_wait(&full[i % VSTAGES], (i / VSTAGES) & 1))
@@ -177,11 +179,14 @@ __global__ void __launch_bounds__(VTHREADS, 1)
                 tc_fence_after();
                 const uint32_t a = smem_addr(smem + (size_t)s * SB);
                 const uint64_t adesc = smem_desc_sw128(a);
-                const uint64_t bdesc = smem_desc_sw128(a + kABytes);
 #pragma unroll
-                for (int k = 0; k < VBK / VUK; ++k)
-                    umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
-                              (t > t0 || k > 0) ? 1u : 0u);
+                for (int piece = 0; piece < 2; ++piece) {
+                    const uint64_t bdesc = smem_desc_sw128(a + kABytes + piece * kBBytes);
+#pragma unroll
+                    for (int k = 0; k < VBK / VUK; ++k)
+                        umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
+                                  (t > t0 || piece > 0 || k > 0) ? 1u : 0u);
+                }
                 umma_commit(&empty[s]);
             }
             umma_commit(&accf[b]);  // chunk complete (or, after an abort, idle)
