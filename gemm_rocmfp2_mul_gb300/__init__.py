@@ -69,6 +69,7 @@ _SIGNATURES = {
     "hfp4_gemv_workspace_bytes": (_SZ, [_I64, _I64]),
     "hfp4_gemv": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
     "rfp2_pack_weights": (_I32, [_P, _I64, _I64, _P, _P]),
+    "rfp2_pack_weights_weighted": (_I32, [_P, _I64, _I64, _P, _P, _P]),
     "hfp4_pack_weights": (_I32, [_P, _I64, _I64, _P, _P, _P]),
     "rfp2_validate_weights": (_I32, [_P, _I64, _P, _P, _P]),
     "rfp2_debug_half_partials": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P]),
@@ -315,6 +316,22 @@ def rfp2_pack_weights(W, out=None):
     M, K = W.shape
     out = _empty((M, K // 32, 10), torch.uint8, W) if out is None else _need(out, torch.uint8, "out")
     _check(lib().rfp2_pack_weights(_ptr(W), M, K, _ptr(out), _stream()), "rfp2_pack_weights")
+    return out
+
+
+def rfp2_pack_weights_weighted(W, importance, out=None):
+    """fp32 W [M, K] and importance fp32 [K] -> ROCmFP2 blocks uint8 [M, K/32, 10]
+    with the importance-weighted scale search."""
+    torch = _torch()
+    _need(W, torch.float32, "W")
+    _need(importance, torch.float32, "importance")
+    M, K = W.shape
+    if importance.numel() != K:
+        raise ValueError("importance needs one value per column")
+    out = (_empty((M, K // 32, 10), torch.uint8, W) if out is None
+           else _need(out, torch.uint8, "out"))
+    _check(lib().rfp2_pack_weights_weighted(_ptr(W), M, K, _ptr(importance), _ptr(out),
+                                            _stream()), "rfp2_pack_weights_weighted")
     return out
 
 

@@ -77,6 +77,69 @@ __global__ void __launch_bounds__(256) rfp2_pack_kernel(const float *__restrict_
     o[8 + half] = (uint8_t)best;
 }
 
+// Importance-weighted scale search ("ROCmFP2 codebook research report",
+// section "05 Completed experiment"): every term of the squared error is
+// weighted by importance_k * sqrt(sigma^2 + x_k^2), sigma^2 = twice the mean
+// of x^2 over the 32-weight block (the page leaves sigma^2 undefined); the
+// same IEEE fp64 steps in the same order as the plain search, one thread per
+// half.  The block, the codebook and the code rule are unchanged.
+__global__ void __launch_bounds__(256) rfp2_pack_weighted_kernel(const float *__restrict__ W,
+                                                                 const float *__restrict__ imp,
+                                                                 int64_t nhalves, int K,
+                                                                 uint8_t *__restrict__ out) {
+    const int64_t h = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (h >= nhalves) return;
+    const int64_t blk = h >> 1, half = h & 1;
+    // sigma^2 over the whole block, summed in index order
+    const float4 *b4 = reinterpret_cast<const float4 *>(W + blk * 32);
+    float xb[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 t = b4[i];
+        xb[4 * i] = t.x;
+        xb[4 * i + 1] = t.y;
+        xb[4 * i + 2] = t.z;
+        xb[4 * i + 3] = t.w;
+    }
+    double s2 = 0.0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) s2 = __dadd_rn(s2, __dmul_rn((double)xb[i], (double)xb[i]));
+    const double sigma2 = __ddiv_rn(__dmul_rn(2.0, s2), 32.0);
+    float x[16];
+    double w[16];
+    const int k0 = (int)((blk * 32) % K) + 16 * (int)half;  // column of element 0 of the half
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        x[i] = xb[16 * half + i];
+        const double xx = __dmul_rn((double)x[i], (double)x[i]);
+        w[i] = __dmul_rn((double)imp[k0 + i], __dsqrt_rn(__dadd_rn(sigma2, xx)));
+    }
+    int best = 0;
+    double best_sse = 0.0;
+    for (int b = 0; b <= 0x7E; ++b) {
+        const float s = ue4m3_scale(b);
+        double sse = 0.0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float r = __fmul_rn(level_of(code_of(x[i], s)), s);
+            const double e = __dsub_rn((double)x[i], (double)r);
+            sse = __dadd_rn(sse, __dmul_rn(w[i], __dmul_rn(e, e)));
+        }
+        if (b == 0 || sse < best_sse) {
+            best_sse = sse;
+            best = b;
+        }
+    }
+    const float s = ue4m3_scale(best);
+    uint32_t word = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) word |= (uint32_t)code_of(x[i], s) << (2 * i);
+    uint8_t *o = out + blk * 10;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[4 * half + i] = (uint8_t)(word >> (8 * i));
+    o[8 + half] = (uint8_t)best;
+}
+
 // Scale bytes >= 0x7F.
 __global__ void rfp2_validate_kernel(const uint8_t *__restrict__ W, int64_t nblocks,
                                      unsigned long long *bad, int32_t *status) {
@@ -202,6 +265,22 @@ extern "C" rfp2_status rfp2_pack_weights(const float *W, int64_t M, int64_t K, u
     if (ctas > 0x7FFFFFFF) return RFP2_ESHAPE;
     return from_cuda(launch(rfp2_pack_kernel, dim3((unsigned)ctas), dim3(256), 0,
                             reinterpret_cast<cudaStream_t>(stream), false, W, nh, out));
+}
+
+extern "C" rfp2_status rfp2_pack_weights_weighted(const float *W, int64_t M, int64_t K,
+                                                  const float *importance, uint8_t *out,
+                                                  rfp2_stream_t stream) {
+    if (M < 0 || K < 0) return RFP2_EINVAL;
+    if (K % 32 != 0 || K > 0x7FFFFFFF) return RFP2_ESHAPE;
+    if (M == 0 || K == 0) return RFP2_OK;
+    if (!W || !importance || !out) return RFP2_EINVAL;
+    if (!aligned(W, 16) || !aligned(importance, 4)) return RFP2_EALIGN;
+    const int64_t nh = M * K / 16;
+    const int64_t ctas = (nh + 255) / 256;
+    if (ctas > 0x7FFFFFFF) return RFP2_ESHAPE;
+    return from_cuda(launch(rfp2_pack_weighted_kernel, dim3((unsigned)ctas), dim3(256), 0,
+                            reinterpret_cast<cudaStream_t>(stream), false, W, importance, nh,
+                            (int)K, out));
 }
 
 extern "C" rfp2_status hfp4_pack_weights(const float *W, int64_t M, int64_t K, uint8_t *out,

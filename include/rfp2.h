@@ -246,6 +246,23 @@ rfp2_status hfp4_gemv(const uint8_t *W, int64_t M, int64_t K, const float *x, in
                       rfp2_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * rfp2_pack_weights with the importance-weighted scale search ("ROCmFP2
+ * codebook research report", section "05 Completed experiment": the squared
+ * reconstruction error of every candidate scale has each term weighted by
+ * importance_k * sqrt(sigma^2 + x_k^2); the page leaves sigma^2 undefined and
+ * it is taken as twice the mean of x^2 over the 32-weight block).  Same block,
+ * codebook and code rule; only the chosen scale bytes can differ.  Ties keep
+ * the smaller byte; a half whose importance is all zero gets byte 0x00.
+ *   W fp32 [M, K] device, 16-byte aligned; importance fp32 [K] device, one
+ *   finite value >= 0 per input column (e.g. mean squared activation);
+ *   out uint8 [M, K/32, 10] device.
+ * Errors: EINVAL, ESHAPE (K % 32), EALIGN, ECUDA.
+ */
+rfp2_status rfp2_pack_weights_weighted(const float *W, int64_t M, int64_t K,
+                                       const float *importance, uint8_t *out,
+                                       rfp2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Weight packers (offline preparation; "02 Quantization" for ROCmFP2 and
  * "Quantization recipe (HFP4G32)" for HFP4).  Output is bit-identical to the
  * CPU oracle's packers.

@@ -63,6 +63,9 @@ def _load():
                 "orc_rfp2_half_sse": (C.c_double, [P, C.c_int]),
                 "orc_rfp2_quantize_half": (C.c_int, [P, P]),
                 "orc_rfp2_pack": (C.c_int, [P, I64, I64, P]),
+                "orc_rfp2_pack_weighted": (C.c_int, [P, I64, I64, P, P]),
+                "orc_rfp2_half_wsse": (C.c_double, [P, P, C.c_double, C.c_int]),
+                "orc_rfp2_block_sigma2": (C.c_double, [P]),
                 "orc_rfp2_decode": (C.c_int, [P, I64, I64, P]),
                 "orc_rfp2_count_bad_scales": (I64, [P, I64]),
                 "orc_quantize_act": (C.c_int, [P, I64, I64, P, P]),
@@ -145,6 +148,31 @@ def rfp2_pack(W: np.ndarray) -> np.ndarray:
     out = np.zeros((M, K // 32, 10), np.uint8)
     _check(_load().orc_rfp2_pack(_ptr(W), M, K, _ptr(out)), "rfp2_pack")
     return out
+
+
+def rfp2_pack_weighted(W: np.ndarray, importance: np.ndarray) -> np.ndarray:
+    """fp32 W [M, K] and importance fp32 [K] -> uint8 [M, K/32, 10] with the
+    importance-weighted scale search (same block, codebook and code rule)."""
+    W = _c(W, np.float32)
+    imp = _c(importance, np.float32).reshape(-1)
+    M, K = W.shape
+    if imp.size != K:
+        raise ValueError("importance needs one value per column")
+    out = np.zeros((M, K // 32, 10), np.uint8)
+    _check(_load().orc_rfp2_pack_weighted(_ptr(W), M, K, _ptr(imp), _ptr(out)),
+           "rfp2_pack_weighted")
+    return out
+
+
+def rfp2_half_wsse(x16: np.ndarray, imp16: np.ndarray, sigma2: float, b: int) -> float:
+    """Weighted squared error of one 16-value half at scale byte b."""
+    return float(_load().orc_rfp2_half_wsse(_ptr(_c(x16, np.float32)), _ptr(_c(imp16, np.float32)),
+                                            float(sigma2), int(b)))
+
+
+def rfp2_block_sigma2(x32: np.ndarray) -> float:
+    """sigma^2 of the weighted objective: twice the mean of x^2 over the block."""
+    return float(_load().orc_rfp2_block_sigma2(_ptr(_c(x32, np.float32))))
 
 
 def rfp2_decode(P: np.ndarray, M: int, K: int) -> np.ndarray:

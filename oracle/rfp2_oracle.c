@@ -146,6 +146,82 @@ int orc_rfp2_pack(const float *W, int64_t M, int64_t K, uint8_t *out)
     return ORC_OK;
 }
 
+/* Importance-weighted scale search ([R] "05 Completed experiment": the same
+ * squared reconstruction error with each term weighted by
+ * importance_i * sqrt(sigma^2 + x_i^2); only the chosen scale changes, not
+ * the block, the codebook or the code rule).  The page does not define
+ * sigma^2; it is read as twice the mean of x^2 over the 32-weight block.
+ * Terms are summed in index order in fp64: w_i * (e_i * e_i). */
+double orc_rfp2_block_sigma2(const float *x32)
+{
+    double s2 = 0.0;
+    for (int i = 0; i < 32; i++) s2 = s2 + (double)x32[i] * (double)x32[i];
+    return 2.0 * s2 / 32.0;
+}
+
+double orc_rfp2_half_wsse(const float *x, const float *imp, double sigma2, int b)
+{
+    double sd;
+    if (orc_ue4m3(b, &sd) != ORC_OK) return INFINITY;
+    float s = (float)sd;
+    double sse = 0.0;
+    for (int i = 0; i < 16; i++) {
+        int code = orc_rfp2_code(x[i], s);
+        float r = (float)orc_codebook[code] * s;
+        double e = (double)x[i] - (double)r;
+        double w = (double)imp[i] * sqrt(sigma2 + (double)x[i] * (double)x[i]);
+        sse = sse + w * (e * e);
+    }
+    return sse;
+}
+
+/* Weighted search of one half: ascending bytes, first strict minimum. */
+int orc_rfp2_quantize_half_weighted(const float *x, const float *imp, double sigma2,
+                                    uint8_t *codes)
+{
+    int best = 0;
+    double best_sse = orc_rfp2_half_wsse(x, imp, sigma2, 0);
+    for (int b = 1; b <= 0x7E; b++) {
+        double sse = orc_rfp2_half_wsse(x, imp, sigma2, b);
+        if (sse < best_sse) {
+            best_sse = sse;
+            best = b;
+        }
+    }
+    double sd;
+    orc_ue4m3(best, &sd);
+    for (int i = 0; i < 16; i++) codes[i] = (uint8_t)orc_rfp2_code(x[i], (float)sd);
+    return best;
+}
+
+/* orc_rfp2_pack with the weighted search; importance fp32 [K] (one value per
+ * input column, finite and >= 0). */
+int orc_rfp2_pack_weighted(const float *W, int64_t M, int64_t K, const float *imp, uint8_t *out)
+{
+    if (M < 0 || K < 0 || K % 32 != 0) return ORC_EINVAL;
+    for (int64_t i = 0; i < M * K; i++)
+        if (!isfinite(W[i])) return ORC_EINVAL;
+    for (int64_t k = 0; k < K; k++)
+        if (!isfinite(imp[k]) || imp[k] < 0.0f) return ORC_EINVAL;
+    int64_t nb = K / 32;
+    for (int64_t m = 0; m < M; m++) {
+        for (int64_t j = 0; j < nb; j++) {
+            const float *x = W + m * K + 32 * j;
+            uint8_t *blk = out + (m * nb + j) * 10;
+            uint8_t codes[32];
+            double sigma2 = orc_rfp2_block_sigma2(x);
+            int e0 = orc_rfp2_quantize_half_weighted(x, imp + 32 * j, sigma2, codes);
+            int e1 = orc_rfp2_quantize_half_weighted(x + 16, imp + 32 * j + 16, sigma2, codes + 16);
+            memset(blk, 0, 8);
+            for (int i = 0; i < 32; i++)
+                blk[i / 4] |= (uint8_t)(codes[i] << (2 * (i % 4)));
+            blk[8] = (uint8_t)e0;
+            blk[9] = (uint8_t)e1;
+        }
+    }
+    return ORC_OK;
+}
+
 /* Code of weight i (0..31) of a block and the scale byte of its half. */
 static int blk_code(const uint8_t *blk, int i) { return (blk[i / 4] >> (2 * (i % 4))) & 3; }
 static int blk_scale_byte(const uint8_t *blk, int i) { return blk[8 + i / 16]; }

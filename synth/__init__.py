@@ -170,3 +170,13 @@ def hfp4_gemv(M: int = 8192, K: int = 8192, N: int = 1, seed: int = 4) -> Worklo
     x = normal_activations(r_x, max(N, 8), K)[:N].copy()
     return Workload(f"W=N(0,0.02^2)[{M},{K}], x=N(0,1)[{N},{K}], seed={seed}",
                     W=normal_weights(r_w, M, K, 0.02), x=x)
+
+
+def imatrix_importance(K: int, seed: int = 7, rows: int = 64) -> np.ndarray:
+    """Synthetic importance per input column (an importance matrix stands in
+    for calibration statistics): the mean of a^2 over `rows` activation rows
+    whose channel scales are log-normal exp(N(0, 0.5^2)); fp32 [K]."""
+    r_s, r_a = child_rngs(seed, 2)
+    scale = np.exp(r_s.normal(0.0, 0.5, K))
+    a = r_a.standard_normal((rows, K)) * scale
+    return (a * a).mean(axis=0).astype(np.float32)

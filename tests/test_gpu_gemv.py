@@ -142,6 +142,20 @@ def test_rfp2_pack_tiny_config_bit_exact(g):
 
 
 @pytest.mark.parametrize("kind", ["normal", "student_t", "tiny", "huge", "sparse"])
+def test_rfp2_pack_weighted_bit_exact(g, kind):
+    """Importance-weighted scale search ("05 Completed experiment"): packed
+    bytes equal the oracle's, with synthetic importance, one-hot importance
+    and all-zero importance."""
+    from synth import imatrix_importance
+    W = _weights(kind, 48, 512, seed=21)
+    imp = imatrix_importance(512)
+    for importance in (imp, np.eye(1, 512, 37, dtype=np.float32).ravel() * 3.0,
+                       np.zeros(512, np.float32)):
+        Pg = g.rfp2_pack_weights_weighted(dev(W), dev(importance.astype(np.float32)))
+        np.testing.assert_array_equal(host(Pg), oracle.rfp2_pack_weighted(W, importance))
+
+
+@pytest.mark.parametrize("kind", ["normal", "student_t", "tiny", "huge", "sparse"])
 def test_hfp4_pack_bit_exact(g, kind):
     W = _weights(kind, 48, 1024, seed=5)
     st = status_tensor()

@@ -340,3 +340,89 @@ def test_synth_bf16_cast_matches_torch():
     x = np.random.default_rng(3).normal(0, 1, 4096).astype(np.float32) * 20
     ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     np.testing.assert_array_equal(float32_to_bf16_bits(x), ref)
+
+
+# -- importance-weighted scale search ("05 Completed experiment") ----------------
+
+def _ue4m3_values():
+    return [oracle.ue4m3(b) for b in range(0x7F)]
+
+
+def test_weighted_pack_equals_plain_pack_for_flat_blocks():
+    """With importance 1 and every |x| of a block equal, each term's weight
+    importance * sqrt(sigma^2 + x^2) is one constant per block, so the
+    weighted search has the plain search's minimiser."""
+    rng = np.random.default_rng(11)
+    M, K = 6, 256
+    mags = np.repeat(rng.uniform(1e-3, 0.3, (M, K // 32)), 32, axis=1)
+    W = (mags * rng.choice([-1.0, 1.0], (M, K))).astype(np.float32)
+    P = oracle.rfp2_pack_weighted(W, np.ones(K, np.float32))
+    np.testing.assert_array_equal(P, oracle.rfp2_pack(W))
+
+
+def test_weighted_pack_is_invariant_to_power_of_two_importance_scaling():
+    from synth import imatrix_importance
+    rng = np.random.default_rng(12)
+    W = (rng.standard_normal((5, 512)) * 0.02).astype(np.float32)
+    imp = imatrix_importance(512)
+    P = oracle.rfp2_pack_weighted(W, imp)
+    for k in (-20, -3, 5):
+        np.testing.assert_array_equal(oracle.rfp2_pack_weighted(W, np.ldexp(imp, k)), P)
+
+
+def test_weighted_pack_one_hot_importance_makes_that_weight_exact():
+    """All importance on one weight of each half: the objective is zero exactly
+    at the bytes whose level grid holds that weight, so the smallest such byte
+    wins."""
+    scales = _ue4m3_values()
+    rng = np.random.default_rng(13)
+    K = 64
+    W = (rng.standard_normal((1, K)) * 0.05).astype(np.float32)
+    imp = np.zeros(K, np.float32)
+    targets = {}
+    for h in range(K // 16):
+        i0 = 16 * h + int(rng.integers(16))
+        b0 = int(rng.integers(8, 0x7F))
+        W[0, i0] = np.float32(rng.choice([-4.0, -1.0, 1.0, 4.0]) * scales[b0])
+        imp[i0] = 1.0
+        x = float(W[0, i0])
+        zero = [b for b in range(0x7F) if scales[b] > 0 and
+                (abs(x) == scales[b] or abs(x) == 4 * scales[b])]
+        targets[h] = min(zero)
+    P = oracle.rfp2_pack_weighted(W, imp)
+    for h, b in targets.items():
+        assert P[0, h // 2, 8 + h % 2] == b
+
+
+def test_weighted_pack_zero_importance_picks_the_first_byte():
+    W = (np.random.default_rng(14).standard_normal((2, 64)) * 0.1).astype(np.float32)
+    P = oracle.rfp2_pack_weighted(W, np.zeros(64, np.float32))
+    assert np.all(P[..., 8:] == 0)
+
+
+def test_weighted_pack_never_loses_on_its_own_objective():
+    """Per half, the weighted search's choice has a weighted error no larger
+    than the plain search's choice (and the plain choice is likewise never
+    worse on the plain error)."""
+    from synth import imatrix_importance
+    rng = np.random.default_rng(15)
+    M, K = 4, 256
+    W = (rng.standard_t(5, (M, K)) * 0.02).astype(np.float32)
+    imp = imatrix_importance(K)
+    Pw, Pp = oracle.rfp2_pack_weighted(W, imp), oracle.rfp2_pack(W)
+    better = 0
+    for m in range(M):
+        for j in range(K // 32):
+            x32 = W[m, 32 * j:32 * j + 32]
+            s2 = oracle.rfp2_block_sigma2(x32)
+            acc = 0.0
+            for v in x32.astype(np.float64):
+                acc += v * v
+            assert s2 == 2.0 * acc / 32.0
+            for h in range(2):
+                x, w = x32[16 * h:16 * h + 16], imp[32 * j + 16 * h:32 * j + 16 * h + 16]
+                ew = oracle.rfp2_half_wsse(x, w, s2, int(Pw[m, j, 8 + h]))
+                ep = oracle.rfp2_half_wsse(x, w, s2, int(Pp[m, j, 8 + h]))
+                assert ew <= ep
+                better += ew < ep
+    assert better > 0
