@@ -12,13 +12,15 @@
 //     per 32-weight block, 64 bytes written per block).  The HFP4G32 variant
 //     (hfp4_gemm) expands E2M1 x 2^(e-127) the same way and leaves the f16
 //     row scale to the GEMM's epilogue.
-//  2. gemm: one CTA per 128-token x 256-weight-row tile.  Warp 0 loads
-//     K-major 64-element slices of both operands with 2-D TMA (SWIZZLE_128B)
-//     into a 4-stage ring; one thread of warp 1 issues tcgen05.mma kind::f16
-//     (M=128, N=256, K=16, bf16 in, fp32 accumulate in tensor memory) and
-//     frees each stage with tcgen05.commit; warps 2-5 read the 128 x 256
-//     accumulator back with tcgen05.ld (each warp its 32-lane quarter) and
-//     store fp32 rows.  Every wait is bounded; tensor memory is always freed.
+//  2. gemm: persistent, one CTA per SM walking 128-token x 256-weight-row
+//     tiles.  Warp 0 loads K-major 64-element slices of both operands with
+//     2-D TMA (SWIZZLE_128B) into a 4-stage ring; one thread of warp 1 issues
+//     tcgen05.mma kind::f16 (M=128, N=256, K=16, bf16 in, fp32 accumulate in
+//     tensor memory, two accumulators used in turn) and frees each stage with
+//     tcgen05.commit; warps 2-5 read a finished accumulator back with
+//     tcgen05.ld (each warp its 32-lane quarter) and store fp32 rows while
+//     the next tile's MMAs run.  Every wait is bounded; tensor memory is
+//     always freed.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -42,7 +44,7 @@ constexpr int kABytes = BM * BK * 2;
 constexpr int kBBytes = BN * BK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 6 * 32;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;  // two 256-column accumulators
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
 
 // ---- expand ----------------------------------------------------------------
@@ -104,7 +106,12 @@ __global__ void __launch_bounds__(256) hfp4_expand_bf16_kernel(const uint8_t *__
 }
 
 // ---- GEMM --------------------------------------------------------------------
-// colscale[m]: optional per-weight-row factor applied to every output.
+// Persistent: CTA c takes tiles c, c + G, c + 2G, ... (tile t = token tile
+// t % ntm of weight tile t / ntm, so neighbouring CTAs share weight tiles in
+// L2).  The stage ring runs on across tiles, and the accumulator alternates
+// between two 256-column halves of tensor memory, so the epilogue of one
+// tile overlaps the MMAs of the next.  colscale[m]: optional per-weight-row
+// factor applied to every output.
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                 float *__restrict__ Y, int Ntok, int Mw, int K, const float *__restrict__ colscale,
@@ -114,13 +121,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kStages * kStageBytes);
     uint64_t *empty = full + kStages;
-    uint64_t *accum_bar = empty + kStages;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum_bar + 1);
+    uint64_t *accf = empty + kStages;  // [2] accumulator b complete
+    uint64_t *acce = accf + 2;         // [2] accumulator b read back
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acce + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile_m = blockIdx.x, tile_n = blockIdx.y;
     const int nk = K / BK;
+    const int ntm = (Ntok + BM - 1) / BM, ntn = (Mw + BN - 1) / BN;
+    const int ntiles = ntm * ntn;
 
     if (threadIdx.x == 0) {
         prefetch_tensor_map(&xmap);
@@ -129,7 +138,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(accum_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf[b], 1);
+            mbar_init(&acce[b], 4);  // one arrival per epilogue warp
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -145,55 +157,78 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         // ---- TMA producer
         pdl_wait();  // X and the expanded weights come from earlier kernels
-        int kb = 0;
-        for (; kb < nk; ++kb) {
-            const int s = kb % kStages;
-            if (kb >= kStages && !mbar_wait(&empty[s], ((kb / kStages) - 1) & 1)) {
-                record_status(status, RFP2_ETIMEOUT);
-                *abort_flag = 1;
-                break;
+        int g = 0;   // k-blocks issued by this CTA
+        for (int t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x) {
+            const int tile_m = t % ntm, tile_n = t / ntm;
+            for (int kb = 0; kb < nk; ++kb, ++g) {
+                const int s = g % kStages;
+                if (g >= kStages && !mbar_wait(&empty[s], ((g / kStages) - 1) & 1)) {
+                    record_status(status, RFP2_ETIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                uint8_t *a = smem + (size_t)s * kStageBytes;
+                mbar_arrive_expect_tx(&full[s], kStageBytes);
+                tma_load_2d(a, &xmap, kb * BK, tile_m * BM, &full[s]);
+                tma_load_2d(a + kABytes, &wmap, kb * BK, tile_n * BN, &full[s]);
             }
-            if (*abort_flag) break;
-            uint8_t *a = smem + (size_t)s * kStageBytes;
-            mbar_arrive_expect_tx(&full[s], kStageBytes);
-            tma_load_2d(a, &xmap, kb * BK, tile_m * BM, &full[s]);
-            tma_load_2d(a + kABytes, &wmap, kb * BK, tile_n * BN, &full[s]);
         }
         // copies still in flight must land before the CTA retires
-        for (int i = max(0, kb - kStages); i < kb; ++i)
+        for (int i = max(0, g - kStages); i < g; ++i)
             if (!mbar_wait(&full[i % kStages], (i / kStages) & 1)) record_status(status, RFP2_ETIMEOUT);
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
         constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kStages;
-            if (*abort_flag || !mbar_wait(&full[s], (kb / kStages) & 1)) {
+        int g = 0, it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
+            const int b = it & 1;
+            if (it >= 2 && (*abort_flag || !mbar_wait(&acce[b], ((it >> 1) - 1) & 1))) {
                 record_status(status, RFP2_ETIMEOUT);
                 *abort_flag = 1;
                 break;
             }
             tc_fence_after();
-            const uint32_t a = smem_addr(smem + (size_t)s * kStageBytes);
-            const uint64_t adesc = smem_desc_sw128(a);
-            const uint64_t bdesc = smem_desc_sw128(a + kABytes);
+            const uint32_t d_tmem = tmem + (uint32_t)(b * BN);
+            for (int kb = 0; kb < nk; ++kb, ++g) {
+                const int s = g % kStages;
+                if (*abort_flag || !mbar_wait(&full[s], (g / kStages) & 1)) {
+                    record_status(status, RFP2_ETIMEOUT);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a = smem_addr(smem + (size_t)s * kStageBytes);
+                const uint64_t adesc = smem_desc_sw128(a);
+                const uint64_t bdesc = smem_desc_sw128(a + kABytes);
 #pragma unroll
-            for (int k = 0; k < BK / UK; ++k)
-                umma_bf16(tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-            umma_commit(&empty[s]);  // the stage is free once these MMAs complete
+                for (int k = 0; k < BK / UK; ++k)
+                    umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
+                              (kb > 0 || k > 0) ? 1u : 0u);
+                umma_commit(&empty[s]);  // the stage is free once these MMAs complete
+            }
+            umma_commit(&accf[b]);  // accumulator complete (or, after an abort, idle)
         }
-        umma_commit(accum_bar);  // accumulator complete (or, after an abort, idle)
     } else if (warp >= 2) {
-        // ---- epilogue: TMEM -> registers -> Y
-        const bool ok = mbar_wait(accum_bar, 0);
-        if (!ok) record_status(status, RFP2_ETIMEOUT);
-        tc_fence_after();
+        // ---- epilogue: TMEM -> registers -> Y, one tile behind the MMAs
         const int q = warp & 3;  // TMEM lanes 32q .. 32q+31
-        const int row = tile_m * BM + q * 32 + lane;
-        if (ok && !*abort_flag) {
+        int it = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+            const int b = it & 1;
+            if (*abort_flag || !mbar_wait(&accf[b], (it >> 1) & 1)) {
+                record_status(status, RFP2_ETIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const int tile_m = t % ntm, tile_n = t / ntm;
+            const int row = tile_m * BM + q * 32 + lane;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + c * 32, r);
+                tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c * 32), r);
                 tmem_ld_wait();
                 const int col0 = tile_n * BN + c * 32;
                 if (row < Ntok) {
@@ -216,6 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[b]);
         }
     }
     tc_fence_before();
@@ -268,7 +306,8 @@ extern "C" rfp2_status rfp2_gemm(const uint8_t *W, int64_t M, int64_t K, const u
             configured[dev] = 1;
         }
     }
-    const dim3 grid((unsigned)((N + BM - 1) / BM), (unsigned)((M + BN - 1) / BN));
+    const int64_t tiles = ((N + BM - 1) / BM) * ((M + BN - 1) / BN);
+    const dim3 grid((unsigned)std::min<int64_t>(tiles, sm_count(dev)));
     return from_cuda(launch(gemm_kernel, grid, dim3(kThreads), kSmemBytes, s, true, xmap, wmap, Y,
                             (int)N, (int)M, (int)K, static_cast<const float *>(nullptr),
                             dev_status));
@@ -321,7 +360,8 @@ extern "C" rfp2_status hfp4_gemm(const uint8_t *W, int64_t M, int64_t K, const u
             configured[dev] = 1;
         }
     }
-    const dim3 grid((unsigned)((N + BM - 1) / BM), (unsigned)((M + BN - 1) / BN));
+    const int64_t tiles = ((N + BM - 1) / BM) * ((M + BN - 1) / BN);
+    const dim3 grid((unsigned)std::min<int64_t>(tiles, sm_count(dev)));
     return from_cuda(launch(gemm_kernel, grid, dim3(kThreads), kSmemBytes, s, true, xmap, wmap, Y,
                             (int)N, (int)M, (int)K, static_cast<const float *>(rs32),
                             dev_status));
