@@ -22,7 +22,9 @@ __all__ = [
     "rfp2_quantize_act", "rfp2_gemv_q8", "rfp2_gemv", "rfp2_gemv_workspace_bytes",
     "rfp2_gemv_noalloc",
     "rfp2_moe_gemv", "rfp2_moe_workspace_bytes", "rfp2_gemm", "rfp2_gemm_workspace_bytes",
-    "hfp4_gemv", "hfp4_gemv_workspace_bytes", "rfp2_pack_weights", "hfp4_pack_weights", "rfp2_validate_weights",
+    "hfp4_gemv", "hfp4_gemv_workspace_bytes", "hfp4_gemm", "hfp4_gemm_workspace_bytes",
+    "rfp2_gemv_batched", "rfp2_gemv_batched_workspace_bytes",
+    "rfp2_pack_weights", "rfp2_pack_weights_weighted", "hfp4_pack_weights", "rfp2_validate_weights",
     "rfp2_debug_half_partials", "rfp2_row_bytes", "hfp4_row_bytes",
 ]
 
