@@ -1,6 +1,6 @@
 // Inline-PTX wrappers for the 5th-generation tensor cores (tcgen05): tensor
 // memory allocation, shared-memory matrix descriptors, the kind::f16 MMA,
-// commit-to-mbarrier and tensor-memory loads.  sm_100a / sm_103a only.
+// commit-to-mbarrier and tensor-memory loads and stores.  sm_100a / sm_103a only.
 #pragma once
 
 #include <stdint.h>
@@ -69,6 +69,31 @@ RFP2_DEV void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (M rows = TMEM lanes, K = 16 f16 as
+// eight 32-bit columns, element 2j in the low half of column j) is read from
+// tensor memory instead of shared memory.
+RFP2_DEV void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                              uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// True in exactly one lane of the (converged) warp.  MMA issue loops run in
+// the whole warp and issue from the elected lane, so that descriptors and
+// addresses stay warp-uniform: issued from one divergent lane, every
+// tcgen05.mma paid for moving its operands to the uniform datapath, about
+// 190 cycles an instruction against 40-130 cycles of tensor work.
+RFP2_DEV bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
 // has completed.
 RFP2_DEV void umma_commit(uint64_t *bar) {
@@ -91,6 +116,40 @@ RFP2_DEV void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[31])
         : "r"(taddr));
 }
+// NC (8 or 16) consecutive fp32 columns of this thread's TMEM lane.
+template <int NC>
+RFP2_DEV void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[NC]) {
+    static_assert(NC == 8 || NC == 16, "8 or 16 columns");
+    if constexpr (NC == 8) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                       "=r"(r[6]), "=r"(r[7])
+                     : "r"(taddr));
+    } else {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+            "%14,%15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+              "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+              "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(taddr));
+    }
+}
 RFP2_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Store 32 consecutive 32-bit columns of this thread's TMEM lane.
+RFP2_DEV void tmem_st_32cols(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+// Wait until this thread's tensor-memory stores have completed.
+RFP2_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 }  // namespace rfp2

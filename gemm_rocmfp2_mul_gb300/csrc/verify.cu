@@ -6,55 +6,100 @@
 // activations; expand each block once and reuse it for every activation
 // column, the mid-range between the GEMV and the GEMM).
 //
-// Four launches chained with programmatic dependent launch:
-//  1. expand: packed blocks -> f16 weights (exact) in the workspace;
-//  2. quantize the tokens (Q8_1 blocks, the same kernel as rfp2_gemv);
-//  3. split: x^ = q * dA scaled by 2^-kc (per token) into two f16 pieces,
-//     hi + lo, relative residual <= 2^-22;
-//  4. vb_gemm: one CTA per 128 weight rows x BNT tokens.  Warp 0 streams
-//     K-major 64-element slices of the weights and of both activation pieces
-//     with 2-D TMA (SWIZZLE_128B) into a ring; one thread of warp 1 issues
-//     tcgen05.mma kind::f16 (M = 128 weight rows, N = BNT tokens, K = 16,
-//     f16 in, fp32 in tensor memory).  The tensor cores' fp32 accumulation
-//     does not round to nearest, which over 2K/16 steps would cost ~1.5e-5
-//     relative; so the product is accumulated in short chunks (16 MMAs)
-//     in two alternating tensor-memory buffers, and warps 2-5 add each
-//     finished chunk into fp32 registers (one weight row per thread, BNT
-//     token sums) while the next chunk runs.  They then store y with 2^kc.
+// Three launches chained with programmatic dependent launch:
+//  1. quantize the tokens (Q8_1 blocks, the same kernel as rfp2_gemv);
+//  2. split: x^ = q * dA scaled by 2^-kc (per token) into two f16 pieces,
+//     hi + lo, relative residual <= 2^-22, written per tile of BNT tokens as
+//     BNT hi rows then BNT lo rows, in the K order in which the decode below
+//     lays out the weights (a fixed permutation inside every 16 values);
+//  3. vb_fused_kernel: one CTA per 128 weight rows x BNT tokens.
+//     - warp 2 streams the packed blocks (128 rows x 8 blocks = 80 bytes a
+//       row per stage) with 2-D TMA; it needs no earlier kernel, so it starts
+//       before the dependency wait;
+//     - sixteen decode warps (four groups of four, one TMEM lane quarter
+//       each; group g takes every fourth 64-value slice, so each group has a
+//       second slice of lookahead in the eight-slot ring) turn every block
+//       into exact f16 levels * scale: per
+//       half one byte table {-4s, -s, +s, +4s} (high bytes of the f16 values,
+//       built from f16(s) with one byte add and one OR) and one PRMT per two
+//       weights, the shared low byte coming from f16(s) itself; the 64-value
+//       slices go straight into tensor memory (tcgen05.st), which the MMA
+//       reads as its A operand: the decoded weights never touch shared
+//       memory or HBM;
+//     - warp 0 streams the activation tile (both pieces, one 2-D TMA box of
+//       2*BNT rows, SWIZZLE_128B);
+//     - warp 1 issues tcgen05.mma kind::f16 (A in TMEM, B in shared memory;
+//       M = 128 weight rows, N = 2*BNT = the tokens' hi and lo pieces, K =
+//       16, fp32 in TMEM), the k-steps alternating between two accumulators.
+//       The tensor cores' fp32 accumulation does not round to nearest (over
+//       K = 4096 in one accumulator ~1.5e-5 relative), so no accumulator
+//       takes more than 128 MMAs before the decode warps add it into fp32
+//       registers (one weight row and a quarter of the tokens per thread,
+//       hi + lo; every 64 stages) and, at the end, store y with 2^kc.
 #include <algorithm>
 #include <mutex>
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
-#include "expand.cuh"
 #include "quantize.cuh"
+#include "rfp2_decode.cuh"
 #include "tcgen05.cuh"
 #include "tma.cuh"
 
 namespace rfp2 {
 namespace {
 
-constexpr int VBM = 128;      // weight rows per tile (UMMA M)
-constexpr int VBK = 64;       // K per stage: one 128-byte swizzle row of f16
-constexpr int VUK = 16;       // K per UMMA instruction
-constexpr int VSTAGES = 4;
-constexpr int VCHUNK = 2;     // stages (2 x 8 MMAs) per tensor-memory accumulation chunk
-constexpr int VTHREADS = 6 * 32;
-constexpr int kABytes = VBM * VBK * 2;
+constexpr int VBM = 128;                    // weight rows per tile (UMMA M, TMEM lanes)
+constexpr int VSTEP = 64;                   // K per MMA stage (four UMMA k-steps of 16)
+constexpr int VUK = 16;                     // K per UMMA instruction
+constexpr int VPK = 256;                    // K per packed-weight stage (8 blocks)
+constexpr int kPRowBytes = VPK / 32 * 10;   // 80 bytes of a row per packed stage
+constexpr int kPStageBytes = VBM * kPRowBytes;
+constexpr int VPSTAGES = 4;
+constexpr int kASlots = 8;                  // TMEM A ring, 32 columns (64 f16) per slot
+constexpr int kACol0 = 256;                 // accumulators in columns 0..255, then the A ring
+constexpr int kTmemCols = 512;
+constexpr int VROUND = 64;                  // MMA stages between two read-backs of the accumulators
+constexpr int kDecodeWarps = 16;
+constexpr int kGroups = kDecodeWarps / 4;   // decode groups (one warp per TMEM lane quarter)
+constexpr int VTHREADS = (4 + kDecodeWarps) * 32;  // 0 B loads, 1 MMA, 2 W loads, 3 idle, 4.. decode
 
-// one stage: the weight slice and both activation pieces of the same K range
+// Activation stages: a multiple of the A slots, because one commit per MMA
+// stage (on the activation stage's barrier) also frees the stage's A slot;
+// every commit holds the issuing thread for ~190 cycles.
 template <int BNT>
-constexpr int stage_bytes() { return kABytes + 2 * BNT * VBK * 2; }
+constexpr int vb_bstages() { return BNT <= 32 ? 16 : 8; }
+// mbarriers (2 per activation stage, 2 per packed stage, 2 per A slot, 3
+// more), the TMEM address and the abort flag
+constexpr int kVbBarrierBytes = 1024;
+static_assert((2 * 16 + 2 * VPSTAGES + 3) * 8 + 8 <= kVbBarrierBytes,
+              "barrier region too small");
 template <int BNT>
-constexpr size_t vb_smem_bytes() { return 1024 + (size_t)VSTAGES * stage_bytes<BNT>() + 256; }
+constexpr int vb_bstage_bytes() { return 2 * BNT * VSTEP * 2; }  // BNT hi rows, BNT lo rows
+// at least 120 KB so that one CTA (and its 512 TMEM columns) owns the SM
+template <int BNT>
+constexpr size_t vb_smem_bytes() {
+    return std::max<size_t>(1024 + (size_t)vb_bstages<BNT>() * vb_bstage_bytes<BNT>() +
+                                (size_t)VPSTAGES * kPStageBytes + kVbBarrierBytes,
+                            120 * 1024);
+}
+
+// Position inside a 16-value group: MMA k-slot s holds the weight (and the
+// activation) of index 4*(s % 4) + r(s / 4), r = (0, 2, 1, 3); the decode
+// below produces the slots in this order.
+__host__ __device__ constexpr int vb_slot_source(int s) {
+    return 4 * (s & 3) + ((((s >> 2) & 1) << 1) | ((s >> 3) & 1));
+}
 
 // x^ = q * dA of token n as two f16 pieces after an exact power-of-two
 // scaling (kc from max 127 * dA, so every scaled value is below 2).  Grid
 // (slices, N); every CTA of a token reads its K/32 scales and writes one
-// slice of hi and lo, row-major [N, K].
+// slice of hi and lo in MMA slot order: xp rows [tile][piece][BNT], K wide.
 __global__ void __launch_bounds__(256) vb_split_kernel(const int8_t *__restrict__ q,
                                                        const float *__restrict__ d, int N, int K,
-                                                       __half *__restrict__ xhi,
-                                                       __half *__restrict__ xlo, int *kc_out) {
+                                                       int bnt, __half *__restrict__ xp,
+                                                       int *kc_out) {
     __shared__ float wmax[8];
     pdl_wait();
     pdl_launch_dependents();
@@ -76,50 +121,100 @@ __global__ void __launch_bounds__(256) vb_split_kernel(const int8_t *__restrict_
     const int per = (K + gridDim.x - 1) / gridDim.x;
     const int k0 = blockIdx.x * per, k1 = min(K, k0 + per);
     const int8_t *qr = q + (int64_t)n * K;
-    for (int k = k0 + threadIdx.x; k < k1; k += blockDim.x) {
+    __half *xhi = xp + ((int64_t)(n / bnt) * 2 * bnt + n % bnt) * K;
+    __half *xlo = xhi + (int64_t)bnt * K;
+    for (int o = k0 + threadIdx.x; o < k1; o += blockDim.x) {
+        const int k = (o & ~15) | vb_slot_source(o & 15);
         const float v = ldexpf((float)qr[k] * dr[k >> 5], -kc);
         const __half h = __float2half_rn(v);
-        xhi[(int64_t)n * K + k] = h;
-        xlo[(int64_t)n * K + k] = __float2half_rn(v - __half2float(h));
+        xhi[o] = h;
+        xlo[o] = __float2half_rn(v - __half2float(h));
+    }
+}
+
+// One 10-byte block -> 16 words of f16 pairs (two UMMA k-steps of 8 columns,
+// half 0 then half 1), each weight = level * scale exactly.  Per half: the
+// f16 of the scale s gives the low byte L (shared by +-s and +-4s: the
+// levels are powers of two) and the high byte hb; the table word holds the
+// high bytes of {-4s, -s, +s, +4s} (4s = exponent + 2 = hb + 8; the sign is
+// bit 7), and a PRMT with selector nibbles (L, code, L, code') writes two
+// finished f16 values.  A zero scale gives an all-zero table and L = 0.
+RFP2_DEV void decode_block_f16(const Block &k, uint32_t *w) {
+    float s0, s1;
+    decode_scale_pair(k.scales, s0, s1);
+    const __half2 hs = __floats2half2_rn(s0, s1);  // low half = s0
+    const uint32_t h2 = *reinterpret_cast<const uint32_t *>(&hs);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const uint32_t hb = (h2 >> (8 + 16 * half)) & 0xFFu;
+        uint32_t t = __byte_perm(h2, 0u, half ? 0x3333u : 0x1111u);
+        t = (t + 0x08000008u) | 0x00008080u;
+        t = hb ? t : 0u;
+        const uint32_t L = half ? 0x06060606u : 0x04040404u;  // byte 4 or 6: low byte of f16(s)
+        const uint32_t c = half ? k.hi : k.lo;
+        const uint32_t sa = ((c << 4) & 0x30303030u) | L;  // (c0, c4)  (c8, c12)
+        const uint32_t sb = (c & 0x30303030u) | L;         // (c2, c6)  (c10, c14)
+        const uint32_t sc = ((c << 2) & 0x30303030u) | L;  // (c1, c5)  (c9, c13)
+        const uint32_t sd = ((c >> 2) & 0x30303030u) | L;  // (c3, c7)  (c11, c15)
+        uint32_t *o = w + 8 * half;
+        o[0] = __byte_perm(t, h2, sa);
+        o[1] = __byte_perm(t, h2, sa >> 16);
+        o[2] = __byte_perm(t, h2, sb);
+        o[3] = __byte_perm(t, h2, sb >> 16);
+        o[4] = __byte_perm(t, h2, sc);
+        o[5] = __byte_perm(t, h2, sc >> 16);
+        o[6] = __byte_perm(t, h2, sd);
+        o[7] = __byte_perm(t, h2, sd >> 16);
     }
 }
 
 template <int BNT>
 __global__ void __launch_bounds__(VTHREADS, 1)
-    vb_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap hmap,
-                   const __grid_constant__ CUtensorMap lmap, float *__restrict__ y, int Mw,
-                   int Ntok, int K, const int *__restrict__ kc, int32_t *status) {
-    constexpr int SB = stage_bytes<BNT>();
-    constexpr uint32_t kTmemCols = 2 * BNT < 32 ? 32 : 2 * BNT;
+    vb_fused_kernel(const __grid_constant__ CUtensorMap pmap, const __grid_constant__ CUtensorMap xmap,
+                    float *__restrict__ y, int Mw, int Ntok, int K, const int *__restrict__ kc,
+                    int32_t *status) {
+    constexpr int SB = vb_bstages<BNT>();
+    constexpr int BB = vb_bstage_bytes<BNT>();
+    static_assert(SB % kASlots == 0, "stage t and t + SB must share an A slot");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)VSTAGES * SB);
-    uint64_t *empty = full + VSTAGES;
-    uint64_t *accf = empty + VSTAGES;  // [2] chunk finished in buffer b
-    uint64_t *acce = accf + 2;         // [2] buffer b read back
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acce + 2);
+    uint8_t *bring = smem;                       // [SB][hi | lo], 1024-aligned tiles
+    uint8_t *pring = smem + (size_t)SB * BB;     // [VPSTAGES][128 rows][80 bytes]
+    // full[s]: MMA stage t (s = t % SB) ready = its activation tile landed
+    // and its A slot (t % 8) written; empty[s]: stage t's MMAs complete (B
+    // stage and A slot free again)
+    uint64_t *bfull = reinterpret_cast<uint64_t *>(pring + (size_t)VPSTAGES * kPStageBytes);
+    uint64_t *bempty = bfull + SB;
+    uint64_t *pfull = bempty + SB;
+    uint64_t *pempty = pfull + VPSTAGES;
+    uint64_t *accf = pempty + VPSTAGES;  // a round of MMAs complete
+    uint64_t *acce = accf + 1;          // the accumulators read back
+    uint64_t *mdone = acce + 1;         // every MMA complete
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mdone + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile_m = blockIdx.x, tile_n = blockIdx.y;
-    const int nk = K / VBK;
-    const int nt = nk;
-    const int nchunks = (nt + VCHUNK - 1) / VCHUNK;
-    constexpr int kBBytes = BNT * VBK * 2;
+    const int NT = K / VSTEP;   // MMA stages
+    const int NP = K / VPK;     // packed-weight stages
+    const int nrounds = (NT + VROUND - 1) / VROUND;
+    constexpr int NB = 2 * BNT;   // MMA N: hi and lo pieces of BNT tokens
 
     if (threadIdx.x == 0) {
-        prefetch_tensor_map(&wmap);
-        prefetch_tensor_map(&hmap);
-        prefetch_tensor_map(&lmap);
-        for (int s = 0; s < VSTAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+        prefetch_tensor_map(&pmap);
+        prefetch_tensor_map(&xmap);
+        for (int s = 0; s < SB; ++s) {
+            mbar_init(&bfull[s], 1 + 4);  // the TMA producer and one warp per TMEM lane quarter
+            mbar_init(&bempty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&accf[b], 1);
-            mbar_init(&acce[b], 4);  // one arrival per epilogue warp
+        for (int s = 0; s < VPSTAGES; ++s) {
+            mbar_init(&pfull[s], 1);
+            mbar_init(&pempty[s], kDecodeWarps);
         }
+        mbar_init(accf, 1);
+        mbar_init(acce, kDecodeWarps);
+        mbar_init(mdone, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -132,98 +227,164 @@ __global__ void __launch_bounds__(VTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 && lane == 0) {
-        // ---- TMA producer: weights (A) and one activation piece (B) per slice
-        pdl_wait();
-        int t = 0;
-        for (; t < nt; ++t) {
-            const int s = t % VSTAGES;
-            if (t >= VSTAGES && !mbar_wait(&empty[s], ((t / VSTAGES) - 1) & 1)) {
-                record_status(status, RFP2_ETIMEOUT);
-                *abort_flag = 1;
-                break;
-            }
-            if (*abort_flag) break;
-            uint8_t *a = smem + (size_t)s * SB;
-            mbar_arrive_expect_tx(&full[s], SB);
-            tma_load_2d(a, &wmap, t * VBK, tile_m * VBM, &full[s]);
-            tma_load_2d(a + kABytes, &hmap, t * VBK, tile_n * BNT, &full[s]);
-            tma_load_2d(a + kABytes + kBBytes, &lmap, t * VBK, tile_n * BNT, &full[s]);
-        }
-        for (int i = max(0, t - VSTAGES); i < t; ++i)
-            if (!mbar_wait(&full[i % VSTAGES], (i / VSTAGES) & 1))
-                record_status(status, RFP2_ETIMEOUT);
-    } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer: chunk c accumulates into buffer c & 1
-        constexpr uint32_t idesc = idesc_f16_f32(VBM, BNT);
-        bool ok = true;
-        for (int c = 0; c < nchunks && ok; ++c) {
-            const int b = c & 1;
-            if (c >= 2 && (*abort_flag || !mbar_wait(&acce[b], ((c >> 1) - 1) & 1))) {
-                record_status(status, RFP2_ETIMEOUT);
-                *abort_flag = 1;
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t d_tmem = tmem + (uint32_t)(b * BNT);
-            const int t0 = c * VCHUNK, t1 = min(nt, t0 + VCHUNK);
-            for (int t = t0; t < t1; ++t) {
-                const int s = t % VSTAGES;
-                if (*abort_flag || !mbar_wait(&full[s], (t / VSTAGES) & 1)) {
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- activation pieces (written by the split kernel)
+            pdl_wait();
+            int t = 0;
+            for (; t < NT; ++t) {
+                const int s = t % SB;
+                if (t >= SB && !mbar_wait(&bempty[s], ((t / SB) - 1) & 1)) {
                     record_status(status, RFP2_ETIMEOUT);
                     *abort_flag = 1;
-                    ok = false;
                     break;
                 }
-                tc_fence_after();
-                const uint32_t a = smem_addr(smem + (size_t)s * SB);
-                const uint64_t adesc = smem_desc_sw128(a);
-#pragma unroll
-                for (int piece = 0; piece < 2; ++piece) {
-                    const uint64_t bdesc = smem_desc_sw128(a + kABytes + piece * kBBytes);
-#pragma unroll
-                    for (int k = 0; k < VBK / VUK; ++k)
-                        umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
-                                  (t > t0 || piece > 0 || k > 0) ? 1u : 0u);
-                }
-                umma_commit(&empty[s]);
+                if (*abort_flag) break;
+                mbar_arrive_expect_tx(&bfull[s], BB);
+                tma_load_2d(bring + (size_t)s * BB, &xmap, t * VSTEP, tile_n * NB, &bfull[s]);
             }
-            umma_commit(&accf[b]);  // chunk complete (or, after an abort, idle)
+            for (int i = max(0, t - SB); i < t; ++i)
+                if (!mbar_wait(&bfull[i % SB], (i / SB) & 1)) record_status(status, RFP2_ETIMEOUT);
         }
-    } else if (warp >= 2) {
-        // ---- epilogue: add every finished chunk into fp32 registers
-        const int q = warp & 3;  // tensor-memory lanes 32q .. 32q+31 = weight rows
-        const int m = tile_m * VBM + q * 32 + lane;
-        float acc[BNT];
-#pragma unroll
-        for (int i = 0; i < BNT; ++i) acc[i] = 0.0f;
-        bool ok = true;
-        for (int c = 0; c < nchunks; ++c) {
-            const int b = c & 1;
-            if (*abort_flag || !mbar_wait(&accf[b], (c >> 1) & 1)) {
-                record_status(status, RFP2_ETIMEOUT);
+    } else if (warp == 2) {
+        if (lane == 0) {
+            // ---- packed weights: no earlier kernel writes them
+            int p = 0;
+            for (; p < NP; ++p) {
+                const int s = p % VPSTAGES;
+                if (p >= VPSTAGES && !mbar_wait(&pempty[s], ((p / VPSTAGES) - 1) & 1)) {
+                    record_status(status, RFP2_ETIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                mbar_arrive_expect_tx(&pfull[s], kPStageBytes);
+                tma_load_2d(pring + (size_t)s * kPStageBytes, &pmap, p * kPRowBytes, tile_m * VBM,
+                            &pfull[s]);
+            }
+            for (int i = max(0, p - VPSTAGES); i < p; ++i)
+                if (!mbar_wait(&pfull[i % VPSTAGES], (i / VPSTAGES) & 1))
+                    record_status(status, RFP2_ETIMEOUT);
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer (the whole warp; one elected lane issues): stage t
+        // reads A slot t % 8 and B stage t % SB; k-step kk goes to
+        // accumulator kk & 1; round r = stages [64r, 64r + 64) starts both
+        // afresh.  An mbarrier probe costs ~100 cycles even when the phase
+        // is complete, so the next stage's probe is issued before this
+        // stage's MMAs, and the abort flag is read only every 8 stages.
+        constexpr uint32_t idesc = idesc_f16_f32(VBM, NB);
+        const uint64_t bdesc0 = smem_desc_sw128(smem_addr(bring));
+        const uint32_t a_tmem0 = tmem + (uint32_t)kACol0;
+        bool ready = NT > 0 && mbar_try_wait(&bfull[0], 0);
+        for (int t = 0; t < NT; ++t) {
+            const int r = t / VROUND, as = t % kASlots, bs = t % SB;
+            const bool fresh = t % VROUND == 0;
+            bool bad = (t % 8 == 0) && *abort_flag;
+            bad = bad || (fresh && r >= 1 && !mbar_wait(acce, (r - 1) & 1));
+            bad = bad || (!ready && !mbar_wait(&bfull[bs], (t / SB) & 1));
+            if (__any_sync(0xffffffffu, bad)) {  // the lanes leave together
+                if (lane == 0) record_status(status, RFP2_ETIMEOUT);
                 *abort_flag = 1;
-                ok = false;
                 break;
             }
             tc_fence_after();
+            ready = t + 1 < NT && mbar_try_wait(&bfull[(t + 1) % SB], ((t + 1) / SB) & 1);
+            const uint32_t a_tmem = a_tmem0 + (uint32_t)(as * 32);
+            const uint64_t bdesc = bdesc0 + (uint64_t)((bs * BB) >> 4);
+            if (elect_one()) {
 #pragma unroll
-            for (int j = 0; j < BNT / 32; ++j) {
-                uint32_t r[32];
-                tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BNT + j * 32), r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) acc[j * 32 + i] += __uint_as_float(r[i]);
+                for (int kk = 0; kk < VSTEP / VUK; ++kk)
+                    umma_f16_tmem_a(tmem + (uint32_t)((kk & 1) * NB), a_tmem + 8 * kk,
+                                    bdesc + 2 * kk, idesc, (fresh && kk < 2) ? 0u : 1u);
+                umma_commit(&bempty[bs]);  // frees B stage bs and A slot as
+                if (t % VROUND == VROUND - 1 || t == NT - 1) umma_commit(accf);
             }
+            __syncwarp();
+        }
+        if (elect_one()) umma_commit(mdone);
+        __syncwarp();
+        if (!mbar_wait(mdone, 0) && lane == 0) record_status(status, RFP2_ETIMEOUT);
+    } else if (warp >= 4) {
+        // ---- decode: group g takes slice g of every packed stage (stage t =
+        // 4p + g), then reads back its quarter of the tokens
+        const int g = (warp - 4) >> 2, q = warp & 3;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const uint8_t *prow = pring + (size_t)(32 * q + lane) * kPRowBytes + 20 * g;
+        constexpr int TQ = BNT / kGroups;  // tokens read back by this thread
+        float acc[TQ];
+#pragma unroll
+        for (int i = 0; i < TQ; ++i) acc[i] = 0.0f;
+        bool ok = true;
+        int drained = 0;  // rounds read back so far
+        auto drain = [&](int r) {
+            if (*abort_flag || !mbar_wait(accf, r & 1)) {
+                record_status(status, RFP2_ETIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int piece = 0; piece < 2; ++piece) {
+                    uint32_t v[TQ];
+                    tmem_ld_cols<TQ>(lane_base + tmem + (uint32_t)(j * NB + piece * BNT + g * TQ), v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < TQ; ++i) acc[i] += __uint_as_float(v[i]);
+                }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acce[b]);
-        }
-        if (ok && m < Mw) {
+            if (lane == 0) mbar_arrive(acce);
+            return true;
+        };
+        for (int t = g; t < NT && ok; t += kGroups) {
+            // entering round r + 1: read back round r first (its MMAs need
+            // nothing more from this group; the next round's wait for it)
+            if (t >= (drained + 1) * VROUND) {
+                if (!drain(drained)) { ok = false; break; }
+                ++drained;
+            }
+            const int p = t / 4, ps = p % VPSTAGES, as = t % kASlots;
+            if (*abort_flag || !mbar_wait(&pfull[ps], (p / VPSTAGES) & 1)) {
+                record_status(status, RFP2_ETIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            // this slice's 20 bytes of the row: blocks 2g and 2g + 1 of the stage
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(prow + (size_t)ps * kPStageBytes);
+            uint32_t v[5];
 #pragma unroll
-            for (int i = 0; i < BNT; ++i) {
-                const int n = tile_n * BNT + i;
+            for (int i = 0; i < 5; ++i) v[i] = src[i];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pempty[ps]);
+            // slot as was last read by MMA stage t - 8: its B stage's barrier
+            if (t >= kASlots && (*abort_flag || !mbar_wait(&bempty[(t - kASlots) % SB],
+                                                            ((t - kASlots) / SB) & 1))) {
+                record_status(status, RFP2_ETIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            uint32_t w[32];
+            decode_block_f16(block_from_words<2>(v, 0), w);
+            decode_block_f16(block_from_words<2>(v, 1), w + 16);
+            tmem_st_32cols(tmem + lane_base + (uint32_t)(kACol0 + as * 32), w);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bfull[t % SB]);
+        }
+        if (ok && !*abort_flag) {
+            while (drained < nrounds && drain(drained)) ++drained;
+        }
+        pdl_wait();  // kc comes from the split kernel
+        const int m = tile_m * VBM + q * 32 + lane;
+        if (drained == nrounds && m < Mw) {
+#pragma unroll
+            for (int i = 0; i < TQ; ++i) {
+                const int n = tile_n * BNT + g * TQ + i;
                 if (n < Ntok) y[(int64_t)n * Mw + m] = acc[i] * ldexpf(1.0f, kc[n]);
             }
         }
@@ -237,29 +398,27 @@ __global__ void __launch_bounds__(VTHREADS, 1)
 }
 
 struct VbWs {
-    __half *wexp;
     int8_t *q;
     float *d;
-    __half *xhi, *xlo;
+    __half *xp;  // [tiles][hi | lo][BNT][K]
     int *kc;
     size_t bytes;
 };
+
+int64_t vb_bnt(int64_t N) { return N <= 32 ? 32 : 64; }
+int64_t vb_tiles_n(int64_t N) { return (N + vb_bnt(N) - 1) / vb_bnt(N); }
 
 VbWs carve_vb(void *ws, int64_t M, int64_t K, int64_t N) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     uint8_t *p = static_cast<uint8_t *>(ws);
     VbWs w;
     size_t o = 0;
-    w.wexp = reinterpret_cast<__half *>(p + o);
-    o += up((size_t)M * K * 2);
     w.q = reinterpret_cast<int8_t *>(p + o);
     o += up((size_t)N * K);
     w.d = reinterpret_cast<float *>(p + o);
     o += up((size_t)N * (K / 32) * 4);
-    w.xhi = reinterpret_cast<__half *>(p + o);
-    o += up((size_t)N * K * 2);
-    w.xlo = reinterpret_cast<__half *>(p + o);
-    o += up((size_t)N * K * 2);
+    w.xp = reinterpret_cast<__half *>(p + o);
+    o += up((size_t)vb_tiles_n(N) * 2 * vb_bnt(N) * K * 2);
     w.kc = reinterpret_cast<int *>(p + o);
     o += up((size_t)N * 4);
     w.bytes = o;
@@ -267,15 +426,15 @@ VbWs carve_vb(void *ws, int64_t M, int64_t K, int64_t N) {
 }
 
 template <int BNT>
-cudaError_t launch_vb_gemm(const VbWs &w, float *y, int64_t M, int64_t K, int64_t N,
-                           int32_t *status, cudaStream_t s) {
-    CUtensorMap wmap, hmap, lmap;
-    if (!encode_tensor_map_2d(&wmap, w.wexp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K,
-                              (uint64_t)M, (uint64_t)K * 2, VBK, VBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map_2d(&hmap, w.xhi, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K,
-                              (uint64_t)N, (uint64_t)K * 2, VBK, BNT, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map_2d(&lmap, w.xlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K,
-                              (uint64_t)N, (uint64_t)K * 2, VBK, BNT, CU_TENSOR_MAP_SWIZZLE_128B))
+cudaError_t launch_vb_fused(const uint8_t *W, const VbWs &w, float *y, int64_t M, int64_t K,
+                            int64_t N, int32_t *status, cudaStream_t s) {
+    CUtensorMap pmap, xmap;
+    const uint64_t row_bytes = (uint64_t)(K / 32) * 10;
+    const uint64_t xrows = (uint64_t)vb_tiles_n(N) * 2 * BNT;
+    if (!encode_tensor_map_2d(&pmap, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, (uint64_t)M,
+                              row_bytes, kPRowBytes, VBM) ||
+        !encode_tensor_map_2d(&xmap, w.xp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, xrows,
+                              (uint64_t)K * 2, VSTEP, 2 * BNT, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     static std::mutex mu;
     static int configured[64] = {0};
@@ -283,14 +442,14 @@ cudaError_t launch_vb_gemm(const VbWs &w, float *y, int64_t M, int64_t K, int64_
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 64 && !configured[dev]) {
-            cudaError_t e = set_smem_limit(vb_gemm_kernel<BNT>, (int)vb_smem_bytes<BNT>());
+            cudaError_t e = set_smem_limit(vb_fused_kernel<BNT>, (int)vb_smem_bytes<BNT>());
             if (e != cudaSuccess) return e;
             configured[dev] = 1;
         }
     }
     const dim3 grid((unsigned)((M + VBM - 1) / VBM), (unsigned)((N + BNT - 1) / BNT));
-    return launch(vb_gemm_kernel<BNT>, grid, dim3(VTHREADS), vb_smem_bytes<BNT>(), s, true, wmap,
-                  hmap, lmap, y, (int)M, (int)N, (int)K, static_cast<const int *>(w.kc), status);
+    return launch(vb_fused_kernel<BNT>, grid, dim3(VTHREADS), vb_smem_bytes<BNT>(), s, true, pmap,
+                  xmap, y, (int)M, (int)N, (int)K, static_cast<const int *>(w.kc), status);
 }
 
 }  // namespace
@@ -316,19 +475,14 @@ extern "C" rfp2_status rfp2_gemv_batched(const uint8_t *W, int64_t M, int64_t K,
     if (!aligned(W, 16) || !aligned(x, 4) || !aligned(y, 4) || !aligned(workspace, 256))
         return RFP2_EALIGN;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int64_t nblocks = M * (K / 32);
-    cudaError_t e = launch(expand_kernel<__half>, dim3((unsigned)((nblocks + 255) / 256)),
-                           dim3(256), 0, s, true, W, nblocks, w.wexp);
-    if (e != cudaSuccess) return RFP2_ECUDA;
-    e = launch_quantize(x, N, K, w.q, w.d, s, true);
+    cudaError_t e = launch_quantize(x, N, K, w.q, w.d, s, true);
     if (e != cudaSuccess) return RFP2_ECUDA;
     const int slices = (int)std::min<int64_t>(32, std::max<int64_t>(1, K / 1024));
     e = launch(vb_split_kernel, dim3((unsigned)slices, (unsigned)N), dim3(256), 0, s, true,
                static_cast<const int8_t *>(w.q), static_cast<const float *>(w.d), (int)N, (int)K,
-               w.xhi, w.xlo, w.kc);
+               (int)vb_bnt(N), w.xp, w.kc);
     if (e != cudaSuccess) return RFP2_ECUDA;
-    if (N <= 32) e = launch_vb_gemm<32>(w, y, M, K, N, dev_status, s);
-    else if (N <= 64) e = launch_vb_gemm<64>(w, y, M, K, N, dev_status, s);
-    else e = launch_vb_gemm<128>(w, y, M, K, N, dev_status, s);
+    if (N <= 32) e = launch_vb_fused<32>(W, w, y, M, K, N, dev_status, s);
+    else e = launch_vb_fused<64>(W, w, y, M, K, N, dev_status, s);
     return from_cuda(e);
 }

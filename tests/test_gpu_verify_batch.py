@@ -1,6 +1,6 @@
 """GPU parity of the verify-batch ROCmFP2 GEMV (rfp2_gemv_batched: tensor
-cores, weights expanded once to f16, activations quantized as Q8_1 blocks and
-split into two f16 pieces) against the CPU oracle's int-path GEMV, through
+cores, weights decoded to f16 inside the GEMM kernel, activations quantized as
+Q8_1 blocks and split into two f16 pieces) against the CPU oracle's int-path GEMV, through
 the C ABI.  Bar: the q and d it leaves in the workspace bit-exact; outputs
 within 1e-5 relative, normwise per output row (one token's [M] vector)."""
 import numpy as np
@@ -35,7 +35,7 @@ def host(t):
 
 def _ws_qd(wsh, M, K, N):
     up = lambda v: (v + 255) // 256 * 256
-    o = up(M * K * 2)
+    o = 0
     q = wsh[o:o + N * K].view(np.int8).reshape(N, K)
     o += up(N * K)
     d = wsh[o:o + N * K // 32 * 4].view(np.float32).reshape(N, K // 32)
