@@ -37,6 +37,21 @@ bool encode_tensor_map_2d(CUtensorMap *map, const void *base, CUtensorMapDataTyp
     return r == CUDA_SUCCESS;
 }
 
+bool encode_tensor_map_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
+                          const uint64_t (&dims)[3], const uint64_t (&strides)[2],
+                          const uint32_t (&box)[3], CUtensorMapSwizzle swizzle) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+    if (!fn) return false;
+    cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    cuuint64_t st[2] = {strides[0], strides[1]};
+    cuuint32_t b[3] = {box[0], box[1], box[2]};
+    cuuint32_t elem_strides[3] = {1, 1, 1};
+    const CUresult r = fn(map, dtype, 3, const_cast<void *>(base), d, st, b, elem_strides,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int current_device() {
     int dev = 0;
     cudaGetDevice(&dev);

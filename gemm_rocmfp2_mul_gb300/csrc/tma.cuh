@@ -21,6 +21,14 @@ bool encode_tensor_map_2d(CUtensorMap *map, const void *base, CUtensorMapDataTyp
                           uint32_t box_rows,
                           CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE);
 
+// Encode a 3-D tiled tensor map: dims[0] contiguous elements, byte strides
+// of dims 1 and 2 (multiples of 16), box `box` (box[0] * element size a
+// multiple of 16), zero fill out of bounds.
+bool encode_tensor_map_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
+                          const uint64_t (&dims)[3], const uint64_t (&strides)[2],
+                          const uint32_t (&box)[3],
+                          CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE);
+
 // 2-D tile load (box at element coordinates x = column, y = row) into shared
 // memory, completing on `bar` (transaction bytes = full box, zero-filled out of
 // bounds).  x * element size must be a multiple of 16 bytes.
@@ -29,6 +37,17 @@ RFP2_DEV void tma_load_2d(void *smem_dst, const CUtensorMap *map, int x, int y, 
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// 3-D tile load at element coordinates (x, y, z); x * element size must be a
+// multiple of 16 bytes.
+RFP2_DEV void tma_load_3d(void *smem_dst, const CUtensorMap *map, int x, int y, int z,
+                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
         : "memory");
 }
 

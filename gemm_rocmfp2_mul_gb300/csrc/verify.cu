@@ -56,24 +56,30 @@ constexpr int VUK = 16;                     // K per UMMA instruction
 constexpr int VPK = 256;                    // K per packed-weight stage (8 blocks)
 constexpr int kPRowBytes = VPK / 32 * 10;   // 80 bytes of a row per packed stage
 constexpr int kPStageBytes = VBM * kPRowBytes;
-constexpr int VPSTAGES = 4;
+// Packed-weight stages in flight.
+template <int BNT>
+constexpr int vb_pstages() { return BNT <= 32 ? 8 : 3; }
+constexpr int kMaxPStages = 8;
 constexpr int kASlots = 8;                  // TMEM A ring, 32 columns (64 f16) per slot
 constexpr int kACol0 = 256;                 // accumulators in columns 0..255, then the A ring
 constexpr int kTmemCols = 512;
 constexpr int VROUND = 64;                  // MMA stages between two read-backs of the accumulators
+constexpr int VQ = 4;                       // MMA stages per step of the issuing warp (one packed stage)
 constexpr int kDecodeWarps = 16;
 constexpr int kGroups = kDecodeWarps / 4;   // decode groups (one warp per TMEM lane quarter)
 constexpr int VTHREADS = (4 + kDecodeWarps) * 32;  // 0 B loads, 1 MMA, 2 W loads, 3 idle, 4.. decode
 
-// Activation stages: a multiple of the A slots, because one commit per MMA
-// stage (on the activation stage's barrier) also frees the stage's A slot;
-// every commit holds the issuing thread for ~190 cycles.
+// Activation stages (three steps of VQ).  The issuing warp works in steps of
+// VQ stages with one ready barrier and one commit a step (an mbarrier probe
+// costs ~100 cycles even on a completed phase, a commit ~140), and each
+// step's activation tile arrives as one TMA box: the copy engine keeps few
+// boxes in flight, so its throughput grows with the box.
 template <int BNT>
-constexpr int vb_bstages() { return BNT <= 32 ? 16 : 8; }
+constexpr int vb_bstages() { return 3 * VQ; }
 // mbarriers (2 per activation stage, 2 per packed stage, 2 per A slot, 3
 // more), the TMEM address and the abort flag
 constexpr int kVbBarrierBytes = 1024;
-static_assert((2 * 16 + 2 * VPSTAGES + 3) * 8 + 8 <= kVbBarrierBytes,
+static_assert((2 * 3 + 2 * kMaxPStages + 3) * 8 + 8 <= kVbBarrierBytes,
               "barrier region too small");
 template <int BNT>
 constexpr int vb_bstage_bytes() { return 2 * BNT * VSTEP * 2; }  // BNT hi rows, BNT lo rows
@@ -81,7 +87,7 @@ constexpr int vb_bstage_bytes() { return 2 * BNT * VSTEP * 2; }  // BNT hi rows,
 template <int BNT>
 constexpr size_t vb_smem_bytes() {
     return std::max<size_t>(1024 + (size_t)vb_bstages<BNT>() * vb_bstage_bytes<BNT>() +
-                                (size_t)VPSTAGES * kPStageBytes + kVbBarrierBytes,
+                                (size_t)vb_pstages<BNT>() * kPStageBytes + kVbBarrierBytes,
                             120 * 1024);
 }
 
@@ -175,18 +181,20 @@ __global__ void __launch_bounds__(VTHREADS, 1)
                     int32_t *status) {
     constexpr int SB = vb_bstages<BNT>();
     constexpr int BB = vb_bstage_bytes<BNT>();
-    static_assert(SB % kASlots == 0, "stage t and t + SB must share an A slot");
+    constexpr int QS = SB / VQ;  // step barriers
+    constexpr int VPSTAGES = vb_pstages<BNT>();
+    static_assert(SB % VQ == 0 && kASlots == 2 * VQ && QS >= 3, "step ring");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *bring = smem;                       // [SB][hi | lo], 1024-aligned tiles
     uint8_t *pring = smem + (size_t)SB * BB;     // [VPSTAGES][128 rows][80 bytes]
-    // full[s]: MMA stage t (s = t % SB) ready = its activation tile landed
-    // and its A slot (t % 8) written; empty[s]: stage t's MMAs complete (B
-    // stage and A slot free again)
-    uint64_t *bfull = reinterpret_cast<uint64_t *>(pring + (size_t)VPSTAGES * kPStageBytes);
-    uint64_t *bempty = bfull + SB;
-    uint64_t *pfull = bempty + SB;
+    // fullq[u % QS]: the VQ stages of step u ready (activation tile landed,
+    // A slots written); emptyq[u % QS]: step u's MMAs complete (its B stages
+    // and A slots free again)
+    uint64_t *fullq = reinterpret_cast<uint64_t *>(pring + (size_t)VPSTAGES * kPStageBytes);
+    uint64_t *emptyq = fullq + QS;
+    uint64_t *pfull = emptyq + QS;
     uint64_t *pempty = pfull + VPSTAGES;
     uint64_t *accf = pempty + VPSTAGES;  // a round of MMAs complete
     uint64_t *acce = accf + 1;          // the accumulators read back
@@ -204,9 +212,9 @@ __global__ void __launch_bounds__(VTHREADS, 1)
     if (threadIdx.x == 0) {
         prefetch_tensor_map(&pmap);
         prefetch_tensor_map(&xmap);
-        for (int s = 0; s < SB; ++s) {
-            mbar_init(&bfull[s], 1 + 4);  // the TMA producer and one warp per TMEM lane quarter
-            mbar_init(&bempty[s], 1);
+        for (int s = 0; s < QS; ++s) {
+            mbar_init(&fullq[s], 1 + kDecodeWarps);  // the TMA producer, every decode warp
+            mbar_init(&emptyq[s], 1);
         }
         for (int s = 0; s < VPSTAGES; ++s) {
             mbar_init(&pfull[s], 1);
@@ -229,22 +237,24 @@ __global__ void __launch_bounds__(VTHREADS, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---- activation pieces (written by the split kernel)
+            // ---- activation pieces (written by the split kernel): one box per step
             pdl_wait();
-            int t = 0;
-            for (; t < NT; ++t) {
-                const int s = t % SB;
-                if (t >= SB && !mbar_wait(&bempty[s], ((t / SB) - 1) & 1)) {
+            const int NQ = NT / VQ;
+            int u = 0;
+            for (; u < NQ; ++u) {
+                const int qs = u % QS;
+                if (u >= QS && !mbar_wait(&emptyq[qs], ((u / QS) - 1) & 1)) {
                     record_status(status, RFP2_ETIMEOUT);
                     *abort_flag = 1;
                     break;
                 }
                 if (*abort_flag) break;
-                mbar_arrive_expect_tx(&bfull[s], BB);
-                tma_load_2d(bring + (size_t)s * BB, &xmap, t * VSTEP, tile_n * NB, &bfull[s]);
+                mbar_arrive_expect_tx(&fullq[qs], VQ * BB);
+                tma_load_3d(bring + (size_t)qs * VQ * BB, &xmap, 0, tile_n * NB, u * VQ, &fullq[qs]);
             }
-            for (int i = max(0, t - SB); i < t; ++i)
-                if (!mbar_wait(&bfull[i % SB], (i / SB) & 1)) record_status(status, RFP2_ETIMEOUT);
+            // copies still in flight land before the CTA may exit
+            for (int i = max(0, u - QS); i < u; ++i)
+                if (!mbar_wait(&fullq[i % QS], (i / QS) & 1)) record_status(status, RFP2_ETIMEOUT);
         }
     } else if (warp == 2) {
         if (lane == 0) {
@@ -267,38 +277,44 @@ __global__ void __launch_bounds__(VTHREADS, 1)
                     record_status(status, RFP2_ETIMEOUT);
         }
     } else if (warp == 1) {
-        // ---- MMA issuer (the whole warp; one elected lane issues): stage t
-        // reads A slot t % 8 and B stage t % SB; k-step kk goes to
-        // accumulator kk & 1; round r = stages [64r, 64r + 64) starts both
-        // afresh.  An mbarrier probe costs ~100 cycles even when the phase
-        // is complete, so the next stage's probe is issued before this
-        // stage's MMAs, and the abort flag is read only every 8 stages.
+        // ---- MMA issuer (the whole warp; one elected lane issues): step u =
+        // stages 4u .. 4u+3; stage t reads A slot t % 8 and B stage t % SB,
+        // k-step kk goes to accumulator kk & 1; round r = stages [64r,
+        // 64r + 64) starts both afresh.  The next step's barrier probe is
+        // issued before this step's MMAs; the abort flag is read every other
+        // step.
         constexpr uint32_t idesc = idesc_f16_f32(VBM, NB);
         const uint64_t bdesc0 = smem_desc_sw128(smem_addr(bring));
         const uint32_t a_tmem0 = tmem + (uint32_t)kACol0;
-        bool ready = NT > 0 && mbar_try_wait(&bfull[0], 0);
-        for (int t = 0; t < NT; ++t) {
-            const int r = t / VROUND, as = t % kASlots, bs = t % SB;
-            const bool fresh = t % VROUND == 0;
-            bool bad = (t % 8 == 0) && *abort_flag;
+        const int NQ = NT / VQ;
+        bool ready = NQ > 0 && mbar_try_wait(&fullq[0], 0);
+        for (int u = 0; u < NQ; ++u) {
+            const int qs = u % QS, r = (u * VQ) / VROUND;
+            const bool fresh = (u * VQ) % VROUND == 0;
+            bool bad = (u % 2 == 0) && *abort_flag;
             bad = bad || (fresh && r >= 1 && !mbar_wait(acce, (r - 1) & 1));
-            bad = bad || (!ready && !mbar_wait(&bfull[bs], (t / SB) & 1));
+            bad = bad || (!ready && !mbar_wait(&fullq[qs], (u / QS) & 1));
             if (__any_sync(0xffffffffu, bad)) {  // the lanes leave together
                 if (lane == 0) record_status(status, RFP2_ETIMEOUT);
                 *abort_flag = 1;
                 break;
             }
             tc_fence_after();
-            ready = t + 1 < NT && mbar_try_wait(&bfull[(t + 1) % SB], ((t + 1) / SB) & 1);
-            const uint32_t a_tmem = a_tmem0 + (uint32_t)(as * 32);
-            const uint64_t bdesc = bdesc0 + (uint64_t)((bs * BB) >> 4);
+            ready = u + 1 < NQ && mbar_try_wait(&fullq[(u + 1) % QS], ((u + 1) / QS) & 1);
             if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < VSTEP / VUK; ++kk)
-                    umma_f16_tmem_a(tmem + (uint32_t)((kk & 1) * NB), a_tmem + 8 * kk,
-                                    bdesc + 2 * kk, idesc, (fresh && kk < 2) ? 0u : 1u);
-                umma_commit(&bempty[bs]);  // frees B stage bs and A slot as
-                if (t % VROUND == VROUND - 1 || t == NT - 1) umma_commit(accf);
+                for (int st = 0; st < VQ; ++st) {
+                    const int t = u * VQ + st;
+                    const uint32_t a_tmem = a_tmem0 + (uint32_t)((t % kASlots) * 32);
+                    const uint64_t bdesc = bdesc0 + (uint64_t)(((t % SB) * BB) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < VSTEP / VUK; ++kk)
+                        umma_f16_tmem_a(tmem + (uint32_t)((kk & 1) * NB), a_tmem + 8 * kk,
+                                        bdesc + 2 * kk, idesc,
+                                        (fresh && st == 0 && kk < 2) ? 0u : 1u);
+                }
+                umma_commit(&emptyq[qs]);  // frees the step's B stages and A slots
+                if (((u + 1) * VQ) % VROUND == 0 || u == NQ - 1) umma_commit(accf);
             }
             __syncwarp();
         }
@@ -359,22 +375,23 @@ __global__ void __launch_bounds__(VTHREADS, 1)
             for (int i = 0; i < 5; ++i) v[i] = src[i];
             __syncwarp();
             if (lane == 0) mbar_arrive(&pempty[ps]);
-            // slot as was last read by MMA stage t - 8: its B stage's barrier
-            if (t >= kASlots && (*abort_flag || !mbar_wait(&bempty[(t - kASlots) % SB],
-                                                            ((t - kASlots) / SB) & 1))) {
+            // decode first (overlapping the MMAs still reading the slot),
+            // then wait for slot as, last read by MMA stage t - 8 (step u - 2)
+            uint32_t w[32];
+            decode_block_f16(block_from_words<2>(v, 0), w);
+            decode_block_f16(block_from_words<2>(v, 1), w + 16);
+            const int u = t / VQ;
+            if (u >= 2 && (*abort_flag || !mbar_wait(&emptyq[(u - 2) % QS], ((u - 2) / QS) & 1))) {
                 record_status(status, RFP2_ETIMEOUT);
                 *abort_flag = 1;
                 break;
             }
             tc_fence_after();
-            uint32_t w[32];
-            decode_block_f16(block_from_words<2>(v, 0), w);
-            decode_block_f16(block_from_words<2>(v, 1), w + 16);
             tmem_st_32cols(tmem + lane_base + (uint32_t)(kACol0 + as * 32), w);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bfull[t % SB]);
+            if (lane == 0) mbar_arrive(&fullq[u % QS]);
         }
         if (ok && !*abort_flag) {
             while (drained < nrounds && drain(drained)) ++drained;
@@ -431,10 +448,15 @@ cudaError_t launch_vb_fused(const uint8_t *W, const VbWs &w, float *y, int64_t M
     CUtensorMap pmap, xmap;
     const uint64_t row_bytes = (uint64_t)(K / 32) * 10;
     const uint64_t xrows = (uint64_t)vb_tiles_n(N) * 2 * BNT;
+    // activations as [K/64 slices][rows][64 values]: one box = VQ slices of
+    // the tile's 2*BNT rows, laid out as VQ consecutive SWIZZLE_128B tiles
+    const uint64_t xdims[3] = {(uint64_t)VSTEP, xrows, (uint64_t)(K / VSTEP)};
+    const uint64_t xstrides[2] = {(uint64_t)K * 2, (uint64_t)VSTEP * 2};
+    const uint32_t xbox[3] = {(uint32_t)VSTEP, (uint32_t)(2 * BNT), (uint32_t)VQ};
     if (!encode_tensor_map_2d(&pmap, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, (uint64_t)M,
                               row_bytes, kPRowBytes, VBM) ||
-        !encode_tensor_map_2d(&xmap, w.xp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, xrows,
-                              (uint64_t)K * 2, VSTEP, 2 * BNT, CU_TENSOR_MAP_SWIZZLE_128B))
+        !encode_tensor_map_3d(&xmap, w.xp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xdims, xstrides, xbox,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     static std::mutex mu;
     static int configured[64] = {0};
