@@ -60,8 +60,13 @@ constexpr int kPStageBytes = VBM * kPRowBytes;
 template <int BNT>
 constexpr int vb_pstages() { return BNT <= 32 ? 8 : 3; }
 constexpr int kMaxPStages = 8;
-constexpr int kASlots = 8;                  // TMEM A ring, 32 columns (64 f16) per slot
-constexpr int kACol0 = 256;                 // accumulators in columns 0..255, then the A ring
+// TMEM: the two accumulators (2 x 2*BNT fp32 columns), then the A ring of
+// 32-column slots (64 f16 values of 128 rows) in what is left of the 512
+// columns: three steps of slots at BNT = 32, two at BNT = 64.  The ring depth
+// hides the tensor-memory store of a slot, which competes with the MMAs for
+// tensor memory and waits for the MMAs that last read the slot.
+template <int BNT>
+constexpr int vb_aslots() { return (512 - 4 * BNT) / 32 / 4 * 4; }
 constexpr int kTmemCols = 512;
 constexpr int VROUND = 64;                  // MMA stages between two read-backs of the accumulators
 constexpr int VQ = 4;                       // MMA stages per step of the issuing warp (one packed stage)
@@ -139,38 +144,48 @@ __global__ void __launch_bounds__(256) vb_split_kernel(const int8_t *__restrict_
 }
 
 // One 10-byte block -> 16 words of f16 pairs (two UMMA k-steps of 8 columns,
-// half 0 then half 1), each weight = level * scale exactly.  Per half: the
-// f16 of the scale s gives the low byte L (shared by +-s and +-4s: the
-// levels are powers of two) and the high byte hb; the table word holds the
-// high bytes of {-4s, -s, +s, +4s} (4s = exponent + 2 = hb + 8; the sign is
-// bit 7), and a PRMT with selector nibbles (L, code, L, code') writes two
-// finished f16 values.  A zero scale gives an all-zero table and L = 0.
+// half 0 then half 1), each weight = level * scale exactly.  The decode is
+// bound by the integer pipe, so it is written to keep work off it:
+//  * a UE4M3 scale byte read as E4M3 (sign clear) is 2s, so one cvt and two
+//    packed multiplies give f16(s) and f16(4s) exactly (zero stays zero);
+//  * per half, the high bytes of {-4s, -s, +s, +4s} come from one PRMT of
+//    f16(s), f16(4s) and one OR of the sign bits; the low byte L is shared
+//    by all four (the levels are powers of two) and comes from f16(s);
+//  * a PRMT with selector nibbles (L, code, L, code') then writes two
+//    finished f16 values; the selector shifts are multiplies (the FMA pipe).
+RFP2_DEV uint32_t shl_fma(uint32_t x, uint32_t pow2) { return x * pow2; }
+RFP2_DEV uint32_t shr_fma(uint32_t x, uint32_t pow2_32_minus) { return __umulhi(x, pow2_32_minus); }
+
 RFP2_DEV void decode_block_f16(const Block &k, uint32_t *w) {
-    float s0, s1;
-    decode_scale_pair(k.scales, s0, s1);
-    const __half2 hs = __floats2half2_rn(s0, s1);  // low half = s0
-    const uint32_t h2 = *reinterpret_cast<const uint32_t *>(&hs);
+    uint32_t e2;  // E4M3 values of the two scale bytes: low half byte 0
+    asm("{\n .reg .b16 sc;\n cvt.u16.u32 sc, %1;\n cvt.rn.f16x2.e4m3x2 %0, sc;\n}\n"
+        : "=r"(e2)
+        : "r"(k.scales));
+    // UE4M3 has exponent bias 8: s = E4M3 / 2 and 4s = E4M3 * 2 (both exact)
+    const __half2 e = *reinterpret_cast<const __half2 *>(&e2);
+    const __half2 q1 = __hmul2(e, __float2half2_rn(0.5f));
+    const __half2 q4 = __hmul2(e, __float2half2_rn(2.0f));
+    const uint32_t h2 = *reinterpret_cast<const uint32_t *>(&q1);
+    const uint32_t h4 = *reinterpret_cast<const uint32_t *>(&q4);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-        const uint32_t hb = (h2 >> (8 + 16 * half)) & 0xFFu;
-        uint32_t t = __byte_perm(h2, 0u, half ? 0x3333u : 0x1111u);
-        t = (t + 0x08000008u) | 0x00008080u;
-        t = hb ? t : 0u;
+        // bytes for codes 0..3: hb(4s)|sign, hb(s)|sign, hb(s), hb(4s)
+        const uint32_t t = __byte_perm(h2, h4, half ? 0x7337u : 0x5115u) | 0x00008080u;
         const uint32_t L = half ? 0x06060606u : 0x04040404u;  // byte 4 or 6: low byte of f16(s)
         const uint32_t c = half ? k.hi : k.lo;
-        const uint32_t sa = ((c << 4) & 0x30303030u) | L;  // (c0, c4)  (c8, c12)
-        const uint32_t sb = (c & 0x30303030u) | L;         // (c2, c6)  (c10, c14)
-        const uint32_t sc = ((c << 2) & 0x30303030u) | L;  // (c1, c5)  (c9, c13)
-        const uint32_t sd = ((c >> 2) & 0x30303030u) | L;  // (c3, c7)  (c11, c15)
+        const uint32_t sa = (shl_fma(c, 16u) & 0x30303030u) | L;       // (c0, c4)  (c8, c12)
+        const uint32_t sb = (c & 0x30303030u) | L;                      // (c2, c6)  (c10, c14)
+        const uint32_t sc = (shl_fma(c, 4u) & 0x30303030u) | L;        // (c1, c5)  (c9, c13)
+        const uint32_t sd = (shr_fma(c, 1u << 30) & 0x30303030u) | L;  // (c3, c7)  (c11, c15)
         uint32_t *o = w + 8 * half;
         o[0] = __byte_perm(t, h2, sa);
-        o[1] = __byte_perm(t, h2, sa >> 16);
+        o[1] = __byte_perm(t, h2, shr_fma(sa, 1u << 16));
         o[2] = __byte_perm(t, h2, sb);
-        o[3] = __byte_perm(t, h2, sb >> 16);
+        o[3] = __byte_perm(t, h2, shr_fma(sb, 1u << 16));
         o[4] = __byte_perm(t, h2, sc);
-        o[5] = __byte_perm(t, h2, sc >> 16);
+        o[5] = __byte_perm(t, h2, shr_fma(sc, 1u << 16));
         o[6] = __byte_perm(t, h2, sd);
-        o[7] = __byte_perm(t, h2, sd >> 16);
+        o[7] = __byte_perm(t, h2, shr_fma(sd, 1u << 16));
     }
 }
 
@@ -183,7 +198,11 @@ __global__ void __launch_bounds__(VTHREADS, 1)
     constexpr int BB = vb_bstage_bytes<BNT>();
     constexpr int QS = SB / VQ;  // step barriers
     constexpr int VPSTAGES = vb_pstages<BNT>();
-    static_assert(SB % VQ == 0 && kASlots == 2 * VQ && QS >= 3, "step ring");
+    constexpr int kASlots = vb_aslots<BNT>();
+    constexpr int kACol0 = 4 * BNT;
+    constexpr int AQ = kASlots / VQ;  // steps of lookahead in the A ring
+    static_assert(SB % VQ == 0 && kASlots % VQ == 0 && AQ >= 2 && QS >= 3, "step rings");
+    static_assert(kACol0 + 32 * kASlots <= kTmemCols, "tensor memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -376,12 +395,12 @@ __global__ void __launch_bounds__(VTHREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&pempty[ps]);
             // decode first (overlapping the MMAs still reading the slot),
-            // then wait for slot as, last read by MMA stage t - 8 (step u - 2)
+            // then wait for slot as, last read by MMA stage t - kASlots (step u - AQ)
             uint32_t w[32];
             decode_block_f16(block_from_words<2>(v, 0), w);
             decode_block_f16(block_from_words<2>(v, 1), w + 16);
             const int u = t / VQ;
-            if (u >= 2 && (*abort_flag || !mbar_wait(&emptyq[(u - 2) % QS], ((u - 2) / QS) & 1))) {
+            if (u >= AQ && (*abort_flag || !mbar_wait(&emptyq[(u - AQ) % QS], ((u - AQ) / QS) & 1))) {
                 record_status(status, RFP2_ETIMEOUT);
                 *abort_flag = 1;
                 break;
