@@ -6,13 +6,14 @@
 // activations; expand each block once and reuse it for every activation
 // column, the mid-range between the GEMV and the GEMM).
 //
-// Three launches chained with programmatic dependent launch:
-//  1. quantize the tokens (Q8_1 blocks, the same kernel as rfp2_gemv);
-//  2. split: x^ = q * dA scaled by 2^-kc (per token) into two f16 pieces,
-//     hi + lo, relative residual <= 2^-22, written per tile of BNT tokens as
-//     BNT hi rows then BNT lo rows, in the K order in which the decode below
-//     lays out the weights (a fixed permutation inside every 16 values);
-//  3. vb_fused_kernel: one CTA per 128 weight rows x BNT tokens.
+// Two launches chained with programmatic dependent launch:
+//  1. vb_prep_kernel, one CTA per token: quantize it (Q8_1 blocks, the same
+//     arithmetic as rfp2_gemv), then split x^ = q * dA scaled by 2^-kc into
+//     two f16 pieces, hi + lo, relative residual <= 2^-22, written per tile
+//     of BNT tokens as BNT hi rows then BNT lo rows, in the K order in which
+//     the decode below lays out the weights (a fixed permutation inside
+//     every 16 values);
+//  2. vb_fused_kernel: one CTA per 128 weight rows x BNT tokens.
 //     - warp 2 streams the packed blocks (128 rows x 8 blocks = 80 bytes a
 //       row per stage) with 2-D TMA; it needs no earlier kernel, so it starts
 //       before the dependency wait;
@@ -42,7 +43,6 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
-#include "quantize.cuh"
 #include "rfp2_decode.cuh"
 #include "tcgen05.cuh"
 #include "tma.cuh"
@@ -103,43 +103,100 @@ __host__ __device__ constexpr int vb_slot_source(int s) {
     return 4 * (s & 3) + ((((s >> 2) & 1) << 1) | ((s >> 3) & 1));
 }
 
-// x^ = q * dA of token n as two f16 pieces after an exact power-of-two
-// scaling (kc from max 127 * dA, so every scaled value is below 2).  Grid
-// (slices, N); every CTA of a token reads its K/32 scales and writes one
-// slice of hi and lo in MMA slot order: xp rows [tile][piece][BNT], K wide.
-__global__ void __launch_bounds__(256) vb_split_kernel(const int8_t *__restrict__ q,
-                                                       const float *__restrict__ d, int N, int K,
-                                                       int bnt, __half *__restrict__ xp,
-                                                       int *kc_out) {
+// One CTA per token n (256 threads; thread i owns the 16-value groups
+// g = i, i + 256, ...; a 32-value block is the group pair (2b, 2b + 1), held
+// by neighbouring lanes).  Pass 1 quantizes: d = max|x| / 127 and q =
+// round-half-away(x / d), both IEEE divisions, q and d stored to the
+// workspace.  Then kc = ilogb(127 * max d) (every scaled value below 2) and
+// pass 2 writes x^ = (q * d) * 2^-kc as two f16 pieces in MMA slot order.
+__global__ void __launch_bounds__(256) vb_prep_kernel(const float *__restrict__ x, int K, int bnt,
+                                                      int8_t *__restrict__ q,
+                                                      float *__restrict__ d,
+                                                      __half *__restrict__ xp, int *kc_out) {
     __shared__ float wmax[8];
     pdl_wait();
     pdl_launch_dependents();
-    const int n = blockIdx.y;
-    const int KB = K >> 5;
-    const float *dr = d + (int64_t)n * KB;
+    const int n = blockIdx.x, tid = threadIdx.x;
+    const int G = K >> 4;  // 16-value groups (even: K % 32 == 0)
+    const float *xr = x + (int64_t)n * K;
+    int8_t *qr = q + (int64_t)n * K;
+    float *dr = d + (int64_t)n * (K >> 5);
     float dmax = 0.0f;
-    for (int b = threadIdx.x; b < KB; b += blockDim.x) dmax = fmaxf(dmax, dr[b]);
+    for (int base = 0; base < G; base += 256) {
+        const int g = base + tid;
+        const bool valid = g < G;  // G even and base even: pairs are both valid or both not
+        float v[16];
+        float amax = 0.0f;
+        if (valid) {
+            const float4 *src = reinterpret_cast<const float4 *>(xr + 16 * g);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 f = src[i];
+                v[4 * i] = f.x;
+                v[4 * i + 1] = f.y;
+                v[4 * i + 2] = f.z;
+                v[4 * i + 3] = f.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        if (valid) {
+            const float dd = __fdiv_rn(amax, 127.0f);
+            uint32_t packed[4] = {0u, 0u, 0u, 0u};
+            if (dd != 0.0f) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float r = roundf(__fdiv_rn(v[i], dd));
+                    r = fminf(fmaxf(r, -127.0f), 127.0f);
+                    packed[i >> 2] |= ((uint32_t)(int)r & 0xFFu) << (8 * (i & 3));
+                }
+            }
+            *reinterpret_cast<uint4 *>(qr + 16 * g) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            if ((g & 1) == 0) dr[g >> 1] = dd;
+            dmax = fmaxf(dmax, dd);
+        }
+    }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1)
         dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, off));
-    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = dmax;
-    __syncthreads();
+    if ((tid & 31) == 0) wmax[tid >> 5] = dmax;
+    __syncthreads();  // also publishes q and d to the whole CTA
     dmax = 0.0f;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) dmax = fmaxf(dmax, wmax[i]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dmax = fmaxf(dmax, wmax[i]);
     const float bound = 127.0f * dmax;  // >= max |q * dA| of the token
     const int kc = bound > 0.0f ? ilogbf(bound) : 0;
-    if (threadIdx.x == 0 && blockIdx.x == 0) kc_out[n] = kc;
-    const int per = (K + gridDim.x - 1) / gridDim.x;
-    const int k0 = blockIdx.x * per, k1 = min(K, k0 + per);
-    const int8_t *qr = q + (int64_t)n * K;
+    if (tid == 0) kc_out[n] = kc;
     __half *xhi = xp + ((int64_t)(n / bnt) * 2 * bnt + n % bnt) * K;
     __half *xlo = xhi + (int64_t)bnt * K;
-    for (int o = k0 + threadIdx.x; o < k1; o += blockDim.x) {
-        const int k = (o & ~15) | vb_slot_source(o & 15);
-        const float v = ldexpf((float)qr[k] * dr[k >> 5], -kc);
-        const __half h = __float2half_rn(v);
-        xhi[o] = h;
-        xlo[o] = __float2half_rn(v - __half2float(h));
+    for (int g = tid; g < G; g += 256) {
+        const uint4 qw = *reinterpret_cast<const uint4 *>(qr + 16 * g);
+        const uint32_t qv[4] = {qw.x, qw.y, qw.z, qw.w};
+        const float dd = dr[g >> 1];
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+            const int k = vb_slot_source(s);
+            const int qk = (int)(int8_t)(qv[k >> 2] >> (8 * (k & 3)));
+            const float val = ldexpf((float)qk * dd, -kc);
+            const __half h = __float2half_rn(val);
+            const __half l = __float2half_rn(val - __half2float(h));
+            const uint32_t hb = __half_as_ushort(h), lb = __half_as_ushort(l);
+            if (s & 1) {
+                hi[s >> 1] |= hb << 16;
+                lo[s >> 1] |= lb << 16;
+            } else {
+                hi[s >> 1] = hb;
+                lo[s >> 1] = lb;
+            }
+        }
+        uint4 *ho = reinterpret_cast<uint4 *>(xhi + 16 * g);
+        uint4 *lo4 = reinterpret_cast<uint4 *>(xlo + 16 * g);
+        ho[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        ho[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+        lo4[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        lo4[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
     }
 }
 
@@ -513,15 +570,11 @@ extern "C" rfp2_status rfp2_gemv_batched(const uint8_t *W, int64_t M, int64_t K,
     if (K % 256 != 0 || M % 16 != 0) return RFP2_EUNSUPPORTED;
     const VbWs w = carve_vb(workspace, M, K, N);
     if (!workspace || workspace_bytes < w.bytes) return RFP2_EWORKSPACE;
-    if (!aligned(W, 16) || !aligned(x, 4) || !aligned(y, 4) || !aligned(workspace, 256))
+    if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 4) || !aligned(workspace, 256))
         return RFP2_EALIGN;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_quantize(x, N, K, w.q, w.d, s, true);
-    if (e != cudaSuccess) return RFP2_ECUDA;
-    const int slices = (int)std::min<int64_t>(32, std::max<int64_t>(1, K / 1024));
-    e = launch(vb_split_kernel, dim3((unsigned)slices, (unsigned)N), dim3(256), 0, s, true,
-               static_cast<const int8_t *>(w.q), static_cast<const float *>(w.d), (int)N, (int)K,
-               (int)vb_bnt(N), w.xp, w.kc);
+    cudaError_t e = launch(vb_prep_kernel, dim3((unsigned)N), dim3(256), 0, s, true, x, (int)K,
+                           (int)vb_bnt(N), w.q, w.d, w.xp, w.kc);
     if (e != cudaSuccess) return RFP2_ECUDA;
     if (N <= 32) e = launch_vb_fused<32>(W, w, y, M, K, N, dev_status, s);
     else e = launch_vb_fused<64>(W, w, y, M, K, N, dev_status, s);

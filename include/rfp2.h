@@ -195,8 +195,8 @@ rfp2_status rfp2_gemm(const uint8_t *W, int64_t M, int64_t K, const uint16_t *X,
  * pieces (relative residual <= 2^-22), and both pieces are multiplied with
  * fp32 accumulation; each output is within about 1e-6 relative of the exact
  * int-path result.
- *   x fp32 [N, K] device, 1 <= N <= 65535; y fp32 [N, M] device, 16-byte
- *   aligned; W 16-byte aligned; workspace device,
+ *   x fp32 [N, K] device, 16-byte aligned, 1 <= N <= 65535; y fp32 [N, M]
+ *   device; W 16-byte aligned; workspace device,
  *   rfp2_gemv_batched_workspace_bytes(M, K, N) bytes, 256-byte aligned
  *   (q int8 [N, K], then d fp32 [N, K/32], each at a 256-byte boundary, then
  *   the two activation pieces and the per-token exponents).
