@@ -21,6 +21,8 @@
 //     trip).  Expert offsets are 64-bit.
 #include <mutex>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "gemv_core.cuh"
 #include "quantize.cuh"
@@ -125,18 +127,14 @@ __device__ void block_exclusive_scan(int *v, int n, int *warp_sums) {
 // (shorts) and flag (bytes), P entries each.
 size_t route_smem_bytes(int P) { return (size_t)P * (4 + 4 + 4 + 2 + 1) + 16; }
 
-__global__ void __launch_bounds__(kRouteThreads, 1)
-    moe_route_kernel(const int32_t *__restrict__ ids, int P, int64_t E, int M, float *y,
-                     int32_t *status, MoeWs w) {
-    extern __shared__ __align__(16) int rsm[];
+RFP2_DEV void moe_route_body(const int32_t *__restrict__ ids, int P, int64_t E, int M, float *y,
+                            int32_t *status, const MoeWs &w, int *rsm) {
     int *sid = rsm;              // expert of pair p, -1 if invalid
     int *gidx = sid + P;         // by sorted position: group-start flag, then group index
     int *erank = gidx + P;       // by sorted position: expert
     short *left = reinterpret_cast<short *>(erank + P);  // pairs left in the expert run
     unsigned char *flag = reinterpret_cast<unsigned char *>(left + P);
     __shared__ int warp_sums[32];
-    pdl_wait();
-    pdl_launch_dependents();
     const int tid = threadIdx.x;
     int nvalid = 0;
     for (int base = 0; base < P; base += blockDim.x) {
@@ -198,6 +196,24 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
         w.header[0] = nvalid > 0 ? gidx[nvalid - 1] + flag[nvalid - 1] : 0;
         w.header[1] = nvalid;
     }
+}
+
+// One launch for both inputs of the MoE GEMV: CTA 0 routes (the pass above),
+// the other CTAs quantize the tokens, one warp per 32-value block.
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    moe_prep_kernel(const int32_t *__restrict__ ids, int P, int64_t E, int M, float *y,
+                    int32_t *status, MoeWs w, const float *__restrict__ x, int64_t nblocks) {
+    extern __shared__ __align__(16) int rsm[];
+    pdl_wait();
+    pdl_launch_dependents();
+    if (blockIdx.x == 0) {
+        moe_route_body(ids, P, E, M, y, status, w, rsm);
+        return;
+    }
+    const int warps = blockDim.x >> 5;
+    for (int64_t b = (int64_t)(blockIdx.x - 1) * warps + (threadIdx.x >> 5); b < nblocks;
+         b += (int64_t)(gridDim.x - 1) * warps)
+        quantize_block_warp(x, b, threadIdx.x & 31, w.q, w.d);
 }
 
 struct MoeArgs {
@@ -458,16 +474,17 @@ extern "C" rfp2_status rfp2_moe_gemv(const uint8_t *W, int64_t E, int64_t M, int
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 64 && !configured[dev]) {
             if (set_smem_limit(moe_gemv_kernel, 227 * 1024) != cudaSuccess ||
-                set_smem_limit(moe_route_kernel, (int)route_smem_bytes(kMaxPairs)) != cudaSuccess)
+                set_smem_limit(moe_prep_kernel, (int)route_smem_bytes(kMaxPairs)) != cudaSuccess)
                 return RFP2_ECUDA;
             configured[dev] = 1;
         }
     }
-    cudaError_t e = launch(moe_route_kernel, dim3(1), dim3(kRouteThreads),
+    const int64_t nblocks = T * (K / 32);
+    const int64_t qctas = std::min<int64_t>((nblocks + kRouteThreads / 32 - 1) / (kRouteThreads / 32),
+                                            4 * (int64_t)sm_count(dev));
+    cudaError_t e = launch(moe_prep_kernel, dim3((unsigned)(1 + qctas)), dim3(kRouteThreads),
                            route_smem_bytes((int)(T * top_k)), s, true, ids, (int)(T * top_k), E,
-                           (int)M, y, dev_status, w);
-    if (e != cudaSuccess) return RFP2_ECUDA;
-    e = launch_quantize(x, T, K, w.q, w.d, s, true);
+                           (int)M, y, dev_status, w, x, nblocks);
     if (e != cudaSuccess) return RFP2_ECUDA;
     MoeArgs a;
     a.W = W;

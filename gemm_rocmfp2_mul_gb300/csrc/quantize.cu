@@ -23,22 +23,8 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     for (int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < nblocks;
-         b += warps) {
-        const float a = x[b * 32 + lane];
-        float amax = fabsf(a);
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        const float dd = __fdiv_rn(amax, 127.0f);
-        int v = 0;
-        if (dd != 0.0f) {
-            float r = roundf(__fdiv_rn(a, dd));
-            r = fminf(fmaxf(r, -127.0f), 127.0f);
-            v = static_cast<int>(r);
-        }
-        q[b * 32 + lane] = static_cast<int8_t>(v);
-        if (lane == 0) d[b] = dd;
-    }
+         b += warps)
+        quantize_block_warp(x, b, lane, q, d);
 }
 
 cudaError_t launch_quantize(const float *x, int64_t N, int64_t K, int8_t *q, float *d,
