@@ -25,7 +25,7 @@ __all__ = [
     "hfp4_gemv", "hfp4_gemv_workspace_bytes", "hfp4_gemm", "hfp4_gemm_workspace_bytes",
     "rfp2_gemv_batched", "rfp2_gemv_batched_workspace_bytes",
     "rfp2_pack_weights", "rfp2_pack_weights_weighted", "hfp4_pack_weights", "rfp2_validate_weights",
-    "rfp2_debug_half_partials", "rfp2_row_bytes", "hfp4_row_bytes",
+    "rfp2_debug_half_partials", "rfp2_debug_wait_timeout", "rfp2_row_bytes", "hfp4_row_bytes",
 ]
 
 MAX_BATCH = 8
@@ -75,6 +75,7 @@ _SIGNATURES = {
     "hfp4_pack_weights": (_I32, [_P, _I64, _I64, _P, _P, _P]),
     "rfp2_validate_weights": (_I32, [_P, _I64, _P, _P, _P]),
     "rfp2_debug_half_partials": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P]),
+    "rfp2_debug_wait_timeout": (_I32, [_P, _P]),
 }
 
 
@@ -370,3 +371,12 @@ def rfp2_debug_half_partials(W, M, K, q, partials=None):
     _check(lib().rfp2_debug_half_partials(_ptr(W), M, K, _ptr(q), N, _ptr(partials), _stream()),
            "rfp2_debug_half_partials")
     return partials
+
+
+def rfp2_debug_wait_timeout(dev_status):
+    """Run the bounded-wait test hook: dev_status (device int32 [1]) gets
+    RFP2_ETIMEOUT after the library's wait limit."""
+    torch = _torch()
+    _need(dev_status, torch.int32, "dev_status")
+    _check(lib().rfp2_debug_wait_timeout(_ptr(dev_status), _stream()), "rfp2_debug_wait_timeout")
+    return dev_status

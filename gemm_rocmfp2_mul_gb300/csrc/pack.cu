@@ -324,3 +324,29 @@ extern "C" rfp2_status rfp2_debug_half_partials(const uint8_t *W, int64_t M, int
                             reinterpret_cast<cudaStream_t>(stream), false, W, (int)M, (int)K, q,
                             (int)N, partials));
 }
+
+namespace rfp2 {
+namespace {
+
+// One thread waits, with the library's bounded mbarrier wait, on a barrier
+// that nothing ever arrives on: the wait gives up after the time limit and
+// the kernel reports RFP2_ETIMEOUT, as every pipeline kernel does when a
+// partner stops.
+__global__ void debug_wait_kernel(int32_t *status) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        if (!mbar_wait(&bar, 0)) record_status(status, RFP2_ETIMEOUT);
+    }
+}
+
+}  // namespace
+}  // namespace rfp2
+
+extern "C" rfp2_status rfp2_debug_wait_timeout(int32_t *dev_status, rfp2_stream_t stream) {
+    if (!dev_status) return RFP2_EINVAL;
+    if (!rfp2::aligned(dev_status, 4)) return RFP2_EALIGN;
+    return rfp2::from_cuda(rfp2::launch(rfp2::debug_wait_kernel, dim3(1), dim3(32), 0,
+                                        reinterpret_cast<cudaStream_t>(stream), false, dev_status));
+}

@@ -299,6 +299,13 @@ rfp2_status rfp2_validate_weights(const uint8_t *W, int64_t nblocks, int64_t *ba
 rfp2_status rfp2_debug_half_partials(const uint8_t *W, int64_t M, int64_t K, const int8_t *q,
                                      int64_t N, int32_t *partials, rfp2_stream_t stream);
 
+/* Test hook of the failure handling: one thread waits, with the bounded wait
+ * every pipeline kernel uses, on an mbarrier that nothing arrives on.  The
+ * wait gives up after the library's 2-second limit and the kernel stores
+ * RFP2_ETIMEOUT into *dev_status (device int32, required); nothing faults and
+ * the context stays usable.  Errors: EINVAL, EALIGN, ECUDA. */
+rfp2_status rfp2_debug_wait_timeout(int32_t *dev_status, rfp2_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

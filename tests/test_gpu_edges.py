@@ -153,3 +153,18 @@ def test_moe_degenerate_routing(g, E, T, top_k):
     q, d = oracle.quantize_act(x)
     ref = oracle.rfp2_moe(P, E, M, K, ids, q, d)
     assert np.all(rel_err_rows(y.reshape(T * top_k, M), ref.reshape(T * top_k, M)) <= 1e-5)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(g):
+    """A wait on an mbarrier that nothing arrives on gives up after the
+    library's limit and reports RFP2_ETIMEOUT; the next call runs normally."""
+    import time
+    import torch
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    g.rfp2_debug_wait_timeout(st)
+    assert int(host(st)[0]) == 8  # RFP2_ETIMEOUT
+    assert 1.0 < time.time() - t0 < 30.0
+    P, x, ref = _gemv_case(g, 96, 512, 1, seed=5)
+    y = host(g.rfp2_gemv(dev(P), 96, 512, dev(x)))
+    assert np.all(rel_err_rows(y, ref) <= 1e-5)
