@@ -58,6 +58,21 @@ __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
     return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
 
+// Fragment entry (k-step ks, lane group p) of one column: its four elements
+// x * 2^-kc as hi and lo f16 pieces.
+__device__ __forceinline__ uint4 split_entry(const float *xr, int kc, int ks, int p) {
+    const int base = (ks >> 1) * 32 + 8 * p + 4 * (ks & 1);
+    __half h1[4], h2[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float v = ldexpf(xr[base + i], -kc);
+        h1[i] = __float2half_rn(v);
+        h2[i] = __float2half_rn(v - __half2float(h1[i]));
+    }
+    return make_uint4(pack_h2(h1[0], h1[1]), pack_h2(h1[2], h1[3]), pack_h2(h2[0], h2[1]),
+                      pack_h2(h2[2], h2[3]));
+}
+
 // Grid (slices, N): every CTA of column n finds max |x| over the whole column
 // (the column is a few KB and read from L2 by each slice), then writes its
 // slice of the power-of-two-scaled two-piece f16 split, in the B-fragment
@@ -93,20 +108,8 @@ __global__ void __launch_bounds__(256) hfp4_split_kernel(const float *__restrict
     const int entries = (K / 16) * 4;
     const int per = (entries + gridDim.x - 1) / gridDim.x;
     const int e0 = blockIdx.x * per, e1 = min(entries, e0 + per);
-    for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
-        const int ks = e >> 2, p = e & 3;
-        const int base = (ks >> 1) * 32 + 8 * p + 4 * (ks & 1);
-        __half h1[4], h2[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float v = ldexpf(xr[base + i], -kc);
-            h1[i] = __float2half_rn(v);
-            h2[i] = __float2half_rn(v - __half2float(h1[i]));
-        }
-        frag[((int64_t)ks * N + n) * 4 + p] =
-            make_uint4(pack_h2(h1[0], h1[1]), pack_h2(h1[2], h1[3]), pack_h2(h2[0], h2[1]),
-                       pack_h2(h2[2], h2[3]));
-    }
+    for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x)
+        frag[((int64_t)(e >> 2) * N + n) * 4 + (e & 3)] = split_entry(xr, kc, e >> 2, e & 3);
 }
 
 // Eight E2M1 codes (four bytes; in each byte the low nibble is the even
@@ -152,20 +155,26 @@ struct HfpArgs {
     int32_t *status;
     const int *kc;
     const uint4 *frag;
+    const float *x;  // FOLD: the activations themselves
 };
 
 // PAIRED (N <= 4): the two f16 pieces of token n are MMA columns 2n and
 // 2n + 1, so one MMA per k-step covers both; otherwise the columns are the
-// tokens and each piece takes its own MMA.
-template <bool PAIRED>
+// tokens and each piece takes its own MMA.  FOLD (small N * K): the consumer
+// warps build the fragments of the whole K in shared memory themselves (the
+// split kernel's arithmetic), so no split launch precedes the GEMV.
+template <bool PAIRED, bool FOLD>
 __global__ void __launch_bounds__(kThreads, 1)
     hfp4_gemv_kernel(const __grid_constant__ CUtensorMap wmap, HfpArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int S = a.nstages;
     const int bstage_bytes = 64 * a.N * 64;  // 64 k-steps x N columns x 4 lanes x 16 B
     uint8_t *wst = smem;                                        // [S][kWStageBytes]
-    uint8_t *bst = smem + (size_t)S * kWStageBytes;             // [S][bstage_bytes]
-    float *red = reinterpret_cast<float *>(bst + (size_t)S * bstage_bytes);  // [8][4][32][4]
+    uint8_t *bst = smem + (size_t)S * kWStageBytes;             // [S][bstage_bytes], FOLD: [K/16][N][4]
+    const size_t bbytes = FOLD ? (size_t)(a.K / 16) * a.N * 64 : (size_t)S * bstage_bytes;
+    float *red = reinterpret_cast<float *>(bst + bbytes);  // [8][4][32][4]
+    __shared__ int kc_s[RFP2_MAX_BATCH];
+    __shared__ float cmax[kWarps];
     uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(red) + kRedBytes);
     uint64_t *empty = full + S;
     uint64_t *red_bar = empty + S;
@@ -202,17 +211,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the weight tiles do not depend on earlier kernels: start them first
             for (; c < nchunks && c < S; ++c) {
                 const int ks0 = c * 2 * kChunkBlocks;
-                const int bbytes = min(2 * kChunkBlocks, nks - ks0) * a.N * 64;
+                const int bbytes = FOLD ? 0 : min(2 * kChunkBlocks, nks - ks0) * a.N * 64;
                 mbar_arrive_expect_tx(&full[c], kWStageBytes + bbytes);
                 tma_load_2d_hint(wst + (size_t)c * kWStageBytes, &wmap, 4 + c * (kChunkRowBytes / 4),
                                  row0, &full[c], pol);
             }
-            pdl_wait();  // the activation fragments come from the split kernel
-            for (int i = 0; i < c; ++i) {
-                const int ks0 = i * 2 * kChunkBlocks;
-                const int bbytes = min(2 * kChunkBlocks, nks - ks0) * a.N * 64;
-                bulk_g2s(bst + (size_t)i * bstage_bytes, a.frag + (int64_t)ks0 * a.N * 4, bbytes,
-                         &full[i]);
+            if (!FOLD) {
+                pdl_wait();  // the activation fragments come from the split kernel
+                for (int i = 0; i < c; ++i) {
+                    const int ks0 = i * 2 * kChunkBlocks;
+                    const int bbytes = min(2 * kChunkBlocks, nks - ks0) * a.N * 64;
+                    bulk_g2s(bst + (size_t)i * bstage_bytes, a.frag + (int64_t)ks0 * a.N * 4, bbytes,
+                             &full[i]);
+                }
             }
             for (; c < nchunks; ++c) {
                 const int s = c % S;
@@ -223,12 +234,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (*abort_flag) break;
                 const int ks0 = c * 2 * kChunkBlocks;
-                const int bbytes = min(2 * kChunkBlocks, nks - ks0) * a.N * 64;
+                const int bbytes = FOLD ? 0 : min(2 * kChunkBlocks, nks - ks0) * a.N * 64;
                 mbar_arrive_expect_tx(&full[s], kWStageBytes + bbytes);
                 tma_load_2d_hint(wst + (size_t)s * kWStageBytes, &wmap, 4 + c * (kChunkRowBytes / 4),
                                  row0, &full[s], pol);
-                bulk_g2s(bst + (size_t)s * bstage_bytes, a.frag + (int64_t)ks0 * a.N * 4, bbytes,
-                         &full[s]);
+                if (!FOLD)
+                    bulk_g2s(bst + (size_t)s * bstage_bytes, a.frag + (int64_t)ks0 * a.N * 4, bbytes,
+                             &full[s]);
             }
             for (int i = max(0, c - S); i < c; ++i)
                 if (!mbar_wait(&full[i % S], (i / S) & 1)) record_status(a.status, RFP2_ETIMEOUT);
@@ -239,6 +251,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ consumers
     pdl_wait();
     pdl_launch_dependents();
+    if constexpr (FOLD) {
+        // per column: kc from max |x| (scaled values below 2), then every
+        // fragment entry of the whole K
+        const int ct = threadIdx.x;  // 0 .. kWarps*32-1
+        for (int n = 0; n < a.N; ++n) {
+            const float *xr = a.x + (int64_t)n * a.K;
+            float amax = 0.0f;
+            for (int k = ct; k < a.K; k += kWarps * 32) amax = fmaxf(amax, fabsf(xr[k]));
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            if (lane == 0) cmax[warp] = amax;
+            named_bar_sync(1, kWarps * 32);
+            if (ct == 0) {
+                float m = 0.0f;
+                for (int w = 0; w < kWarps; ++w) m = fmaxf(m, cmax[w]);
+                kc_s[n] = m > 0.0f ? ilogbf(m) : 0;
+            }
+            named_bar_sync(1, kWarps * 32);
+        }
+        uint4 *fr = reinterpret_cast<uint4 *>(bst);
+        const int entries = nks * 4 * a.N;
+        for (int e = ct; e < entries; e += kWarps * 32) {
+            const int p = e & 3, n = (e >> 2) % a.N, ks = (e >> 2) / a.N;
+            fr[e] = split_entry(a.x + (int64_t)n * a.K, kc_s[n], ks, p);
+        }
+        named_bar_sync(1, kWarps * 32);
+    }
     const int g = lane >> 2, p = lane & 3;
     float acc[kMaxTiles][4];
 #pragma unroll
@@ -255,7 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
         }
         const uint8_t *ws = wst + (size_t)s * kWStageBytes;
-        const uint4 *bs = reinterpret_cast<const uint4 *>(bst + (size_t)s * bstage_bytes);
+        const uint4 *bs = FOLD ? reinterpret_cast<const uint4 *>(bst) + (size_t)c * 2 * kChunkBlocks * a.N * 4
+                               : reinterpret_cast<const uint4 *>(bst + (size_t)s * bstage_bytes);
 #pragma unroll
         for (int jj = 0; jj < kBlocksPerWarp; ++jj) {
             const int j = warp * kBlocksPerWarp + jj;  // block inside the chunk
@@ -344,14 +385,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             r1 < a.M ? __half2float(*reinterpret_cast<const __half *>(a.W + (int64_t)r1 * a.rb)) : 0.0f;
         if constexpr (PAIRED) {
             if (p < a.N) {
-                const float s0 = ldexpf(1.0f, a.kc[p]);
+                const float s0 = ldexpf(1.0f, FOLD ? kc_s[p] : a.kc[p]);
                 if (r0 < a.M) a.y[(int64_t)p * a.M + r0] = v[0] * rs0 * s0;
                 if (r1 < a.M) a.y[(int64_t)p * a.M + r1] = v[1] * rs1 * s0;
             }
         } else {
             const int c0 = 2 * p, c1 = 2 * p + 1;
-            const float s0 = c0 < a.N ? ldexpf(1.0f, a.kc[c0]) : 0.0f;
-            const float s1 = c1 < a.N ? ldexpf(1.0f, a.kc[c1]) : 0.0f;
+            const float s0 = c0 < a.N ? ldexpf(1.0f, FOLD ? kc_s[c0] : a.kc[c0]) : 0.0f;
+            const float s1 = c1 < a.N ? ldexpf(1.0f, FOLD ? kc_s[c1] : a.kc[c1]) : 0.0f;
             if (r0 < a.M) {
                 if (c0 < a.N) a.y[(int64_t)c0 * a.M + r0] = v[0] * rs0 * s0;
                 if (c1 < a.N) a.y[(int64_t)c1 * a.M + r0] = v[1] * rs0 * s1;
@@ -392,24 +433,32 @@ extern "C" rfp2_status hfp4_gemv(const uint8_t *W, int64_t M, int64_t K, const f
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int *kc = static_cast<int *>(workspace);
     uint4 *frag = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(workspace) + 256);
-    // slices of K per column: about 1024 fragment entries (4096 elements) each
-    const int slices = (int)std::min<int64_t>(64, std::max<int64_t>(1, K / 4096));
-    cudaError_t e = launch(hfp4_split_kernel, dim3((unsigned)slices, (unsigned)N), dim3(256), 0, s,
-                           true, x, (int)N, (int)K, kc, frag);
-    if (e != cudaSuccess) return RFP2_ECUDA;
+    // Small N * K: the GEMV builds the fragments itself (no split launch, no
+    // dependency hop); they stay in shared memory for the whole K.
+    const size_t fold_bytes = (size_t)(K / 16) * N * 64;
+    const bool fold = N <= 2 && fold_bytes <= 64 * 1024;
+    if (!fold) {
+        // slices of K per column: about 1024 fragment entries (4096 elements) each
+        const int slices = (int)std::min<int64_t>(64, std::max<int64_t>(1, K / 4096));
+        cudaError_t e = launch(hfp4_split_kernel, dim3((unsigned)slices, (unsigned)N), dim3(256), 0,
+                               s, true, x, (int)N, (int)K, kc, frag);
+        if (e != cudaSuccess) return RFP2_ECUDA;
+    }
     // stages: as many 64-row x 1024-K tiles (plus their fragments) as fit
-    const size_t per_stage = kWStageBytes + (size_t)64 * N * 64;
+    const size_t per_stage = kWStageBytes + (fold ? 0 : (size_t)64 * N * 64);
+    const size_t fixed = (fold ? fold_bytes : 0) + kRedBytes + 256;
     int stages = 4;
-    while (stages > 2 && stages * per_stage + kRedBytes + 256 > 226 * 1024) --stages;
-    const size_t smem = stages * per_stage + kRedBytes + 256;
+    while (stages > 2 && stages * per_stage + fixed > 224 * 1024) --stages;
+    const size_t smem = stages * per_stage + fixed;
     static std::mutex mu;
     static int configured[64] = {0};
     const int dev = current_device();
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 64 && !configured[dev]) {
-            if (set_smem_limit(hfp4_gemv_kernel<true>, 226 * 1024) != cudaSuccess ||
-                set_smem_limit(hfp4_gemv_kernel<false>, 226 * 1024) != cudaSuccess)
+            if (set_smem_limit(hfp4_gemv_kernel<true, false>, 224 * 1024) != cudaSuccess ||
+                set_smem_limit(hfp4_gemv_kernel<false, false>, 224 * 1024) != cudaSuccess ||
+                set_smem_limit(hfp4_gemv_kernel<true, true>, 224 * 1024) != cudaSuccess)
                 return RFP2_ECUDA;
             configured[dev] = 1;
         }
@@ -431,9 +480,13 @@ extern "C" rfp2_status hfp4_gemv(const uint8_t *W, int64_t M, int64_t K, const f
     a.status = dev_status;
     a.kc = kc;
     a.frag = frag;
+    a.x = x;
+    if (fold)
+        return from_cuda(launch(hfp4_gemv_kernel<true, true>, dim3(grid), dim3(kThreads), smem, s,
+                                true, wmap, a));
     if (N <= 4)
-        return from_cuda(
-            launch(hfp4_gemv_kernel<true>, dim3(grid), dim3(kThreads), smem, s, true, wmap, a));
-    return from_cuda(
-        launch(hfp4_gemv_kernel<false>, dim3(grid), dim3(kThreads), smem, s, true, wmap, a));
+        return from_cuda(launch(hfp4_gemv_kernel<true, false>, dim3(grid), dim3(kThreads), smem, s,
+                                true, wmap, a));
+    return from_cuda(launch(hfp4_gemv_kernel<false, false>, dim3(grid), dim3(kThreads), smem, s,
+                            true, wmap, a));
 }
