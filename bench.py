@@ -342,7 +342,8 @@ def run_gpu(args):
         },
         "secondary": dict({
             "decode_batch4": {
-                "workload": "same weights, batch 4 (activation quantize fused)",
+                "workload": "same weights, batch 4 through rfp2_gemv (tensor-core path from "
+                            "3 tokens: prep + decode-into-TMEM GEMM)",
                 "value": round(WEIGHT_BYTES / (ms_b4 * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "us_per_call": round(ms_b4 * 1e3, 3),
                 "frac_of_hbm_peak": round(WEIGHT_BYTES / (ms_b4 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),

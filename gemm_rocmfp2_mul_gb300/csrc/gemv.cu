@@ -27,6 +27,8 @@
 //    mbarriers, never through bar.sync, so no wait can hang.
 #include <mutex>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "gemv_core.cuh"
 #include "quantize.cuh"
@@ -357,9 +359,20 @@ extern "C" rfp2_status rfp2_gemv_q8(const uint8_t *W, int64_t M, int64_t K, cons
                                  reinterpret_cast<cudaStream_t>(stream), false));
 }
 
+// From three tokens on, the tensor-core verify-batch path (decode straight
+// into tensor memory, ~18 us for the 14336 x 4096 decode weights at any N up
+// to 32) beats the dp4a GEMV (19.6 us at N = 3, 44 us at N = 8); both give the
+// int path's result within the 1e-5 bar.  It needs M % 16 == 0 and x 16-byte
+// aligned; its workspace starts with the same q and d.
+static bool use_tensor_path(int64_t M, int64_t N, const void *x) {
+    return N >= 3 && M % 16 == 0 && (x == nullptr || rfp2::aligned(x, 16));
+}
+
 extern "C" size_t rfp2_gemv_workspace_bytes(int64_t N, int64_t K) {
     if (N <= 0 || K <= 0) return 0;
-    return gemv_workspace_bytes(N, K);
+    size_t b = gemv_workspace_bytes(N, K);
+    if (N >= 3) b = std::max(b, rfp2_gemv_batched_workspace_bytes(16, K, N));
+    return b;
 }
 
 extern "C" rfp2_status rfp2_gemv(const uint8_t *W, int64_t M, int64_t K, const float *x,
@@ -368,6 +381,8 @@ extern "C" rfp2_status rfp2_gemv(const uint8_t *W, int64_t M, int64_t K, const f
     if (!W || !x || !y) return RFP2_EINVAL;
     const rfp2_status st = check_gemv_shape(M, K, N);
     if (st != RFP2_OK) return st;
+    if (use_tensor_path(M, N, x))
+        return rfp2_gemv_batched(W, M, K, x, N, y, workspace, workspace_bytes, dev_status, stream);
     if (!workspace || workspace_bytes < gemv_workspace_bytes(N, K)) return RFP2_EWORKSPACE;
     if (!aligned(W, 16) || !aligned(x, 4) || !aligned(y, 4) || !aligned(workspace, 256))
         return RFP2_EALIGN;

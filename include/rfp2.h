@@ -110,8 +110,11 @@ size_t rfp2_gemv_workspace_bytes(int64_t N, int64_t K);
  * ROCmFP2 GEMV from fp32 activations: quantizes x (q then d, written to
  * `workspace`) and runs the GEMV.  For N <= 2 (when the activations fit in
  * shared memory beside a weight ring) the quantization runs inside the GEMV
- * kernel, one launch per call; otherwise it is a separate kernel chained to
- * the GEMV with programmatic dependent launch.  Either way the GEMV starts
+ * kernel, one launch per call.  For 3 <= N <= 8 with M % 16 == 0 and x
+ * 16-byte aligned the call is rfp2_gemv_batched (tensor cores, faster from
+ * three tokens on; within about 1e-6 relative of the int path); otherwise the
+ * quantization is a separate kernel chained to the dp4a GEMV with
+ * programmatic dependent launch.  Either way the GEMV starts
  * streaming W before the kernel enqueued just before it on the stream has
  * finished (x, the workspace and y are touched only after it has), so W must
  * not be written by that preceding kernel: after writing W, synchronize the

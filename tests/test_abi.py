@@ -45,9 +45,13 @@ def test_status_strings_and_version(lib):
 
 def test_workspace_sizes(lib):
     import gemm_rocmfp2_mul_gb300 as g
+    up = lambda v: (v + 255) // 256 * 256
     # q int8 [N, K] rounded up to 256 bytes, then d fp32 [N, K/32]
     assert g.rfp2_gemv_workspace_bytes(1, 4096) == 4096 + 128 * 4
-    assert g.rfp2_gemv_workspace_bytes(3, 256) == 768 + 24 * 4
+    # from three tokens the tensor-core path's layout: the same q and d, then
+    # the two f16 activation pieces of a 32-token tile and the exponents
+    assert g.rfp2_gemv_workspace_bytes(3, 256) == up(768) + up(24 * 4) + up(2 * 32 * 256 * 2) + up(3 * 4)
+    assert g.rfp2_gemv_workspace_bytes(3, 256) == g.rfp2_gemv_batched_workspace_bytes(16, 256, 3)
     assert g.rfp2_gemv_workspace_bytes(0, 256) == 0
 
 
