@@ -379,10 +379,12 @@ extern "C" rfp2_status rfp2_gemv(const uint8_t *W, int64_t M, int64_t K, const f
                                  int64_t N, float *y, void *workspace, size_t workspace_bytes,
                                  int32_t *dev_status, rfp2_stream_t stream) {
     if (!W || !x || !y) return RFP2_EINVAL;
+    if (M <= 0 || K <= 0 || N < 1 || N > RFP2_MAX_BATCH) return RFP2_ESHAPE;
+    // the tensor path has its own limits (no activation staging beside a ring)
+    if (K % 256 == 0 && use_tensor_path(M, N, x))
+        return rfp2_gemv_batched(W, M, K, x, N, y, workspace, workspace_bytes, dev_status, stream);
     const rfp2_status st = check_gemv_shape(M, K, N);
     if (st != RFP2_OK) return st;
-    if (use_tensor_path(M, N, x))
-        return rfp2_gemv_batched(W, M, K, x, N, y, workspace, workspace_bytes, dev_status, stream);
     if (!workspace || workspace_bytes < gemv_workspace_bytes(N, K)) return RFP2_EWORKSPACE;
     if (!aligned(W, 16) || !aligned(x, 4) || !aligned(y, 4) || !aligned(workspace, 256))
         return RFP2_EALIGN;

@@ -44,6 +44,7 @@ def _ws_qd(wsh, M, K, N):
 
 @pytest.mark.parametrize("M,K,N", [
     (256, 1024, 32), (512, 4096, 128), (272, 2048, 37), (1024, 768, 200), (128, 512, 1),
+    (256, 8192, 40), (144, 16384, 5),  # several read-backs of the accumulators along K
 ])
 def test_verify_batch_parity(g, M, K, N):
     import torch
@@ -107,3 +108,16 @@ def test_verify_batch_errors(g):
     with pytest.raises(g.RFP2Error) as e:
         g.rfp2_gemv_batched(dev(np.zeros((12, 8, 10), np.uint8)), 12, 256, x)
     assert e.value.status == 4
+
+
+@pytest.mark.parametrize("N", [3, 8])
+def test_gemv_routes_small_batches_to_tensor_path_long_k(g, N):
+    """rfp2_gemv at 3..8 tokens takes the tensor-core path; K = 16384 gives
+    four accumulator read-backs along K."""
+    M, K = 160, 16384
+    r_w, r_x = child_rngs(N + 99, 2)
+    P = oracle.rfp2_pack(normal_weights(r_w, M, K, 0.02))
+    x = r_x.standard_normal((N, K)).astype(np.float32)
+    y = host(g.rfp2_gemv(dev(P), M, K, dev(x)))
+    q, d = oracle.quantize_act(x)
+    assert np.all(rel_err_rows(y, oracle.rfp2_gemv(P, M, K, q, d)) <= TOL)
