@@ -80,6 +80,31 @@ RFP2_DEV bool mbar_wait(uint64_t *bar, uint32_t parity) {
     }
 }
 
+// ---- clusters ----------------------------------------------------------------
+RFP2_DEV uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Shared::cluster address of the variable at `p`'s offset in CTA `rank` of
+// this cluster.
+RFP2_DEV uint32_t cluster_map(const void *p, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(rank));
+    return a;
+}
+// Arrive on an mbarrier given by its shared::cluster address (any CTA of the
+// cluster).
+RFP2_DEV void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+// All threads of all CTAs of the cluster.
+RFP2_DEV void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
 // 1-D bulk async copy global -> shared; completion is signalled on `bar`
 // (transaction bytes).  Both addresses 16-byte aligned, bytes % 16 == 0.
 RFP2_DEV void bulk_g2s(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {

@@ -12,15 +12,20 @@
 //     per 32-weight block, 64 bytes written per block).  The HFP4G32 variant
 //     (hfp4_gemm) expands E2M1 x 2^(e-127) the same way and leaves the f16
 //     row scale to the GEMM's epilogue.
-//  2. gemm: persistent, one CTA per SM walking 128-token x 256-weight-row
-//     tiles.  Warp 0 loads K-major 64-element slices of both operands with
-//     2-D TMA (SWIZZLE_128B) into a 4-stage ring; one thread of warp 1 issues
-//     tcgen05.mma kind::f16 (M=128, N=256, K=16, bf16 in, fp32 accumulate in
-//     tensor memory, two accumulators used in turn) and frees each stage with
-//     tcgen05.commit; warps 2-5 read a finished accumulator back with
-//     tcgen05.ld (each warp its 32-lane quarter) and store fp32 rows while
-//     the next tile's MMAs run.  Every wait is bounded; tensor memory is
-//     always freed.
+//  2. gemm: persistent over CTA pairs (clusters of two SMs), each pair walking
+//     256-token x 256-weight-row tiles.  In each CTA warp 0 loads its 128
+//     tokens and its 128 of the tile's weight rows, K-major 64-element slices
+//     with 2-D TMA (SWIZZLE_128B) into a 6-stage ring; one thread of the even
+//     CTA issues tcgen05.mma.cta_group::2 kind::f16 (M=256, N=256, K=16, bf16
+//     in, fp32 accumulate) over both CTAs' stages, so each SM stores and reads
+//     only half of the B operand; its commits free the stages of both CTAs and
+//     signal both epilogues.  Warps 2-5 of each CTA read that CTA's 128 rows
+//     of the accumulator back with tcgen05.ld and store fp32 rows while the
+//     next tile's MMAs run in the other of two 256-column accumulators.  When
+//     the last wave of whole tiles would leave most pairs idle (at most half
+//     of them busy), its tiles are split into 256 x 128 halves spread over
+//     twice as many pairs.  Every wait is bounded; tensor memory is always
+//     freed.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -35,17 +40,19 @@
 namespace rfp2 {
 namespace {
 
-constexpr int BM = 128;  // tokens per tile (UMMA M)
-constexpr int BN = 256;  // weight rows per tile (UMMA N)
+constexpr int BM = 128;  // tokens per CTA (TMEM lanes)
+constexpr int PM = 256;  // tokens per CTA pair (UMMA M)
+constexpr int BN = 256;  // weight rows per tile (UMMA N), half of them loaded by each CTA
 constexpr int BK = 64;   // K per stage: one 128-byte swizzle row
 constexpr int UK = 16;   // K per UMMA instruction
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kABytes = BM * BK * 2;
-constexpr int kBBytes = BN * BK * 2;
+constexpr int kBBytes = (BN / 2) * BK * 2;  // this CTA's half of the B operand
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 6 * 32;
 constexpr uint32_t kTmemCols = 512;  // two 256-column accumulators
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
+constexpr int BNH = BN / 2;  // weight rows of a half tile
 
 // ---- expand ----------------------------------------------------------------
 // OCP E2M1 code -> float: magnitude index k = c & 7 is 0 (0), 1 (0.5) or,
@@ -106,60 +113,90 @@ __global__ void __launch_bounds__(256) hfp4_expand_bf16_kernel(const uint8_t *__
 }
 
 // ---- GEMM --------------------------------------------------------------------
-// Persistent: CTA c takes tiles c, c + G, c + 2G, ... (tile t = token tile
-// t % ntm of weight tile t / ntm, so neighbouring CTAs share weight tiles in
-// L2).  The stage ring runs on across tiles, and the accumulator alternates
-// between two 256-column halves of tensor memory, so the epilogue of one
-// tile overlaps the MMAs of the next.  colscale[m]: optional per-weight-row
-// factor applied to every output.
-__global__ void __launch_bounds__(kThreads, 1)
+// Schedule slot t -> output tile of a CTA pair.  Slots below t_full are whole
+// 256-token x 256-weight-row tiles (token tile f % ntm of weight tile f / ntm,
+// f = t); each tile after them takes two slots, one per 128-row half of its
+// weight rows.
+struct Slot {
+    int tile_m, col0;  // token tile of the pair; first weight row (output column)
+    bool half;
+};
+__device__ __forceinline__ Slot slot_tile(int t, int t_full, int ntm) {
+    int f = t, h = 0;
+    const bool half = t >= t_full;
+    if (half) {
+        f = t_full + ((t - t_full) >> 1);
+        h = (t - t_full) & 1;
+    }
+    return Slot{f % ntm, (f / ntm) * BN + h * BNH, half};
+}
+
+// Persistent over CTA pairs (clusters of two): pair p takes slots p, p + P,
+// p + 2P, ...  CTA r of the pair loads tokens [256 tm + 128 r, +128) and
+// weight rows [col0 + r n/2, +n/2) of each K slice into its own ring; the even
+// CTA's MMA thread issues M = 256, N = n (256, or 128 for a half tile) pair
+// MMAs over both CTAs' stages, so each SM reads and stores only its half of
+// the B operand.  D rows of CTA r's tokens land in CTA r's tensor memory,
+// alternating between two 256-column accumulators so the epilogue of one tile
+// overlaps the MMAs of the next.  Barriers: full[s] (even CTA; both CTAs'
+// copies complete on it), empty[s] and accf[b] (both CTAs; pair commits
+// arrive on both), acce[b] (even CTA; the eight epilogue warps of the pair).
+// colscale[m]: optional per-weight-row factor applied to every output.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-                float *__restrict__ Y, int Ntok, int Mw, int K, const float *__restrict__ colscale,
-                int32_t *status) {
+                const __grid_constant__ CUtensorMap wmap_h, float *__restrict__ Y, int Ntok, int Mw,
+                int K, int t_full, const float *__restrict__ colscale, int32_t *status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kStages * kStageBytes);
     uint64_t *empty = full + kStages;
     uint64_t *accf = empty + kStages;  // [2] accumulator b complete
-    uint64_t *acce = accf + 2;         // [2] accumulator b read back
+    uint64_t *acce = accf + 2;         // [2] accumulator b read back (even CTA)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acce + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     const int nk = K / BK;
-    const int ntm = (Ntok + BM - 1) / BM, ntn = (Mw + BN - 1) / BN;
+    const int ntm = (Ntok + PM - 1) / PM, ntn = (Mw + BN - 1) / BN;
     const int ntiles = ntm * ntn;
+    const int nslots = t_full + 2 * (ntiles - t_full);
 
     if (threadIdx.x == 0) {
         prefetch_tensor_map(&xmap);
         prefetch_tensor_map(&wmap);
+        prefetch_tensor_map(&wmap_h);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf[b], 1);
-            mbar_init(&acce[b], 4);  // one arrival per epilogue warp
+            mbar_init(&acce[b], 8);  // one arrival per epilogue warp of the pair
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // barriers of both CTAs initialised before either signals the other
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    int g = 0;  // k-blocks loaded by this CTA (producer thread)
     if (warp == 0 && lane == 0) {
-        // ---- TMA producer
+        // ---- TMA producer (both CTAs)
         pdl_wait();  // X and the expanded weights come from earlier kernels
-        int g = 0;   // k-blocks issued by this CTA
-        for (int t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x) {
-            const int tile_m = t % ntm, tile_n = t / ntm;
+        const uint32_t full0 = cluster_map(&full[0], 0);
+        for (int t = pair; t < nslots && !*abort_flag; t += npairs) {
+            const Slot sl = slot_tile(t, t_full, ntm);
+            const int brows = sl.half ? BNH / 2 : BN / 2;
+            const int arow = sl.tile_m * PM + (int)rank * BM, brow = sl.col0 + (int)rank * brows;
             for (int kb = 0; kb < nk; ++kb, ++g) {
                 const int s = g % kStages;
                 if (g >= kStages && !mbar_wait(&empty[s], ((g / kStages) - 1) & 1)) {
@@ -169,20 +206,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (*abort_flag) break;
                 uint8_t *a = smem + (size_t)s * kStageBytes;
-                mbar_arrive_expect_tx(&full[s], kStageBytes);
-                tma_load_2d(a, &xmap, kb * BK, tile_m * BM, &full[s]);
-                tma_load_2d(a + kABytes, &wmap, kb * BK, tile_n * BN, &full[s]);
+                if (rank == 0) mbar_arrive_expect_tx(&full[s], 2u * (uint32_t)(kABytes + brows * BK * 2));
+                tma_load_2d_pair(a, &xmap, kb * BK, arow, full0 + 8u * s);
+                tma_load_2d_pair(a + kABytes, sl.half ? &wmap_h : &wmap, kb * BK, brow, full0 + 8u * s);
             }
         }
-        // copies still in flight must land before the CTA retires
-        for (int i = max(0, g - kStages); i < g; ++i)
-            if (!mbar_wait(&full[i % kStages], (i / kStages) & 1)) record_status(status, RFP2_ETIMEOUT);
-    } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer
-        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
-        int g = 0, it = 0;
+    } else if (warp == 1 && rank == 0 && lane == 0) {
+        // ---- MMA issuer (even CTA)
+        constexpr uint32_t idesc_full = idesc_bf16_f32(PM, BN), idesc_half = idesc_bf16_f32(PM, BNH);
+        int gm = 0, it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
+        for (int t = pair; t < nslots && ok; t += npairs, ++it) {
             const int b = it & 1;
             if (it >= 2 && (*abort_flag || !mbar_wait(&acce[b], ((it >> 1) - 1) & 1))) {
                 record_status(status, RFP2_ETIMEOUT);
@@ -190,10 +224,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
+            const uint32_t idesc = t >= t_full ? idesc_half : idesc_full;
             const uint32_t d_tmem = tmem + (uint32_t)(b * BN);
-            for (int kb = 0; kb < nk; ++kb, ++g) {
-                const int s = g % kStages;
-                if (*abort_flag || !mbar_wait(&full[s], (g / kStages) & 1)) {
+            for (int kb = 0; kb < nk; ++kb, ++gm) {
+                const int s = gm % kStages;
+                if (*abort_flag || !mbar_wait(&full[s], (gm / kStages) & 1)) {
                     record_status(status, RFP2_ETIMEOUT);
                     *abort_flag = 1;
                     ok = false;
@@ -205,17 +240,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t bdesc = smem_desc_sw128(a + kABytes);
 #pragma unroll
                 for (int k = 0; k < BK / UK; ++k)
-                    umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
-                              (kb > 0 || k > 0) ? 1u : 0u);
-                umma_commit(&empty[s]);  // the stage is free once these MMAs complete
+                    umma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
+                                   (kb > 0 || k > 0) ? 1u : 0u);
+                umma_commit_pair_both(&empty[s]);  // both CTAs' stage s free once these complete
             }
-            umma_commit(&accf[b]);  // accumulator complete (or, after an abort, idle)
+            umma_commit_pair_both(&accf[b]);  // accumulator complete (or, after an abort, idle)
         }
     } else if (warp >= 2) {
-        // ---- epilogue: TMEM -> registers -> Y, one tile behind the MMAs
+        // ---- epilogue (both CTAs): TMEM -> registers -> Y, one tile behind the MMAs
         const int q = warp & 3;  // TMEM lanes 32q .. 32q+31
+        const uint32_t acce0 = cluster_map(&acce[0], 0);
         int it = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        for (int t = pair; t < nslots; t += npairs, ++it) {
             const int b = it & 1;
             if (*abort_flag || !mbar_wait(&accf[b], (it >> 1) & 1)) {
                 record_status(status, RFP2_ETIMEOUT);
@@ -223,14 +259,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const int tile_m = t % ntm, tile_n = t / ntm;
-            const int row = tile_m * BM + q * 32 + lane;
+            const Slot sl = slot_tile(t, t_full, ntm);
+            const int row = sl.tile_m * PM + (int)rank * BM + q * 32 + lane;
+            const int nchunks = (sl.half ? BNH : BN) / 32;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < nchunks; ++c) {
                 uint32_t r[32];
                 tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c * 32), r);
                 tmem_ld_wait();
-                const int col0 = tile_n * BN + c * 32;
+                const int col0 = sl.col0 + c * 32;
                 if (row < Ntok) {
                     float4 *dst = reinterpret_cast<float4 *>(Y + (int64_t)row * Mw + col0);
 #pragma unroll
@@ -253,14 +290,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acce[b]);
+            if (lane == 0) mbar_arrive_cluster(acce0 + 8u * b);
+        }
+    }
+    if (warp == 0 && lane == 0) {
+        // The pair commits of the last stages arrive on this CTA's empty
+        // barriers (and the other CTA's copies on the even CTA's full
+        // barriers): neither CTA may leave before they have.  After an abort,
+        // wait for this CTA's own copies instead where it can see them.
+        for (int i = max(0, g - kStages); i < g; ++i) {
+            const bool done = *abort_flag && rank == 0
+                                  ? mbar_wait(&full[i % kStages], (i / kStages) & 1)
+                                  : mbar_wait(&empty[i % kStages], (i / kStages) & 1);
+            if (!done) record_status(status, RFP2_ETIMEOUT);
         }
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc_pair(tmem, kTmemCols);
     }
 }
 
@@ -268,6 +317,56 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace rfp2
 
 using namespace rfp2;
+
+// Whole-tile slots before the split: the last partial wave is split into half
+// tiles when it would occupy at most half of the pairs.
+static int64_t gemm_split_point(int64_t ntiles, int pairs) {
+    const int64_t rem = ntiles % pairs;
+    return (rem > 0 && rem <= pairs / 2) ? ntiles - rem : ntiles;
+}
+
+// Tensor maps for one GEMM launch and the launch itself: one CTA pair per
+// pair of SMs that can hold one at a time (as many as the device reports for
+// this kernel's size), or one per slot when there are fewer slots.
+static rfp2_status launch_gemm(const uint16_t *X, const __nv_bfloat16 *wexp, int64_t N, int64_t M,
+                               int64_t K, float *Y, const float *colscale, int32_t *dev_status,
+                               cudaStream_t s) {
+    CUtensorMap xmap, wmap, wmap_h;
+    if (!encode_tensor_map_2d(&xmap, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K, (uint64_t)N,
+                              (uint64_t)K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_2d(&wmap, wexp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K,
+                              (uint64_t)M, (uint64_t)K * 2, BK, BN / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_2d(&wmap_h, wexp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K,
+                              (uint64_t)M, (uint64_t)K * 2, BK, BNH / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+        return RFP2_ECUDA;
+    static std::mutex mu;
+    static int max_pairs[64] = {0};
+    const int dev = current_device();
+    int pairs = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && max_pairs[dev] > 0) {
+            pairs = max_pairs[dev];
+        } else {
+            if (set_smem_limit(gemm_kernel, (int)kSmemBytes) != cudaSuccess) return RFP2_ECUDA;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = kSmemBytes;
+            if (cudaOccupancyMaxActiveClusters(&pairs, reinterpret_cast<const void *>(gemm_kernel),
+                                               &cfg) != cudaSuccess ||
+                pairs <= 0)
+                return RFP2_ECUDA;
+            if (dev < 64) max_pairs[dev] = pairs;
+        }
+    }
+    const int64_t tiles = ((N + PM - 1) / PM) * ((M + BN - 1) / BN);
+    const int64_t t_full = gemm_split_point(tiles, pairs);
+    const int64_t nslots = t_full + 2 * (tiles - t_full);
+    const dim3 grid((unsigned)(2 * std::min<int64_t>(nslots, pairs)));
+    return from_cuda(launch(gemm_kernel, grid, dim3(kThreads), kSmemBytes, s, true, xmap, wmap, wmap_h,
+                            Y, (int)N, (int)M, (int)K, (int)t_full, colscale, dev_status));
+}
 
 extern "C" size_t rfp2_gemm_workspace_bytes(int64_t M, int64_t K) {
     if (M <= 0 || K <= 0) return 0;
@@ -290,27 +389,7 @@ extern "C" rfp2_status rfp2_gemm(const uint8_t *W, int64_t M, int64_t K, const u
     cudaError_t e = launch(expand_kernel<__nv_bfloat16>, dim3((unsigned)((nblocks + 255) / 256)), dim3(256),
                            0, s, true, W, nblocks, wexp);
     if (e != cudaSuccess) return RFP2_ECUDA;
-    CUtensorMap xmap, wmap;
-    if (!encode_tensor_map_2d(&xmap, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K, (uint64_t)N,
-                              (uint64_t)K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map_2d(&wmap, wexp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K,
-                              (uint64_t)M, (uint64_t)K * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
-        return RFP2_ECUDA;
-    static std::mutex mu;
-    static int configured[64] = {0};
-    const int dev = current_device();
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev < 64 && !configured[dev]) {
-            if (set_smem_limit(gemm_kernel, (int)kSmemBytes) != cudaSuccess) return RFP2_ECUDA;
-            configured[dev] = 1;
-        }
-    }
-    const int64_t tiles = ((N + BM - 1) / BM) * ((M + BN - 1) / BN);
-    const dim3 grid((unsigned)std::min<int64_t>(tiles, sm_count(dev)));
-    return from_cuda(launch(gemm_kernel, grid, dim3(kThreads), kSmemBytes, s, true, xmap, wmap, Y,
-                            (int)N, (int)M, (int)K, static_cast<const float *>(nullptr),
-                            dev_status));
+    return launch_gemm(X, wexp, N, M, K, Y, nullptr, dev_status, s);
 }
 
 // ---- HFP4G32 prefill GEMM ------------------------------------------------------
@@ -344,25 +423,5 @@ extern "C" rfp2_status hfp4_gemm(const uint8_t *W, int64_t M, int64_t K, const u
     cudaError_t e = launch(hfp4_expand_bf16_kernel, dim3((unsigned)((nblocks + 255) / 256)),
                            dim3(256), 0, s, true, W, (int)M, KB, rb, wexp, rs32);
     if (e != cudaSuccess) return RFP2_ECUDA;
-    CUtensorMap xmap, wmap;
-    if (!encode_tensor_map_2d(&xmap, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K, (uint64_t)N,
-                              (uint64_t)K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map_2d(&wmap, wexp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K,
-                              (uint64_t)M, (uint64_t)K * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
-        return RFP2_ECUDA;
-    static std::mutex mu;
-    static int configured[64] = {0};
-    const int dev = current_device();
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev < 64 && !configured[dev]) {
-            if (set_smem_limit(gemm_kernel, (int)kSmemBytes) != cudaSuccess) return RFP2_ECUDA;
-            configured[dev] = 1;
-        }
-    }
-    const int64_t tiles = ((N + BM - 1) / BM) * ((M + BN - 1) / BN);
-    const dim3 grid((unsigned)std::min<int64_t>(tiles, sm_count(dev)));
-    return from_cuda(launch(gemm_kernel, grid, dim3(kThreads), kSmemBytes, s, true, xmap, wmap, Y,
-                            (int)N, (int)M, (int)K, static_cast<const float *>(rs32),
-                            dev_status));
+    return launch_gemm(X, wexp, N, M, K, Y, rs32, dev_status, s);
 }

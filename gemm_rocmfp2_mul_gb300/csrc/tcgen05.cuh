@@ -103,6 +103,44 @@ RFP2_DEV void umma_commit(uint64_t *bar) {
         : "memory");
 }
 
+// ---- CTA pairs (cta_group::2) ----------------------------------------------
+// A kernel uses one cta_group throughout.  In the pair forms one warp of each
+// CTA of a cluster pair allocates (and frees) the same columns in both SMs'
+// tensor memory; one thread of the even CTA issues MMAs whose A rows and B
+// columns are split evenly between the two CTAs' shared memory (same offsets)
+// and whose D rows land in the two CTAs' tensor memory (rows 0..M/2-1 in the
+// even CTA, the rest in the odd one).
+RFP2_DEV void tmem_alloc_pair(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(slot)),
+                 "r"(ncols)
+                 : "memory");
+}
+RFP2_DEV void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+RFP2_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+RFP2_DEV void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                             uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on the barrier at `bar`'s offset in both CTAs of the pair once the
+// pair MMAs issued so far by this thread have completed.
+RFP2_DEV void umma_commit_pair_both(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_addr(bar)),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane (32x32b shape).
 RFP2_DEV void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(

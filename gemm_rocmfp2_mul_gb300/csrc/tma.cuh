@@ -40,6 +40,18 @@ RFP2_DEV void tma_load_2d(void *smem_dst, const CUtensorMap *map, int x, int y, 
         : "memory");
 }
 
+// 2-D tile load into this CTA's shared memory whose completion is signalled
+// on an mbarrier of either CTA of the pair (`bar_cluster`: shared::cluster
+// address, e.g. the even CTA's barrier).
+RFP2_DEV void tma_load_2d_pair(void *smem_dst, const CUtensorMap *map, int x, int y,
+                               uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+
 // 3-D tile load at element coordinates (x, y, z); x * element size must be a
 // multiple of 16 bytes.
 RFP2_DEV void tma_load_3d(void *smem_dst, const CUtensorMap *map, int x, int y, int z,

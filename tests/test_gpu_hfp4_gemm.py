@@ -64,6 +64,9 @@ def test_hfp4_gemm_single_tile(g):
 
 @pytest.mark.parametrize("M,K,N", [
     (512, 1024, 256), (272, 768, 200), (1024, 2048, 130), (256, 5120, 7), (4096, 512, 1000),
+    # 90 tiles of 256 tokens x 256 weight rows: those past the first wave of
+    # CTA pairs run as half tiles, the last weight tile (16 valid rows) among them
+    (4368, 256, 1100),
 ])
 def test_hfp4_gemm_parity(g, M, K, N):
     Y, P, X, _ = _case(g, M, K, N, seed=M + N + K)
