@@ -51,7 +51,9 @@ constexpr int kBBytes = (BN / 2) * BK * 2;  // this CTA's half of the B operand
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 6 * 32;
 constexpr uint32_t kTmemCols = 512;  // two 256-column accumulators
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
+constexpr int kStgStride = 36;  // floats per row of an epilogue warp's 32 x 32 staging tile
+constexpr int kStgFloats = 32 * kStgStride;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 4 * kStgFloats * 4;
 constexpr int BNH = BN / 2;  // weight rows of a half tile
 
 // ---- expand ----------------------------------------------------------------
@@ -247,8 +249,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             umma_commit_pair_both(&accf[b]);  // accumulator complete (or, after an abort, idle)
         }
     } else if (warp >= 2) {
-        // ---- epilogue (both CTAs): TMEM -> registers -> Y, one tile behind the MMAs
+        // ---- epilogue (both CTAs): TMEM -> registers -> Y, one tile behind the MMAs.
+        // Each 32-row x 32-column chunk goes through a padded shared-memory
+        // tile (row = lane on the way in, four rows of 128 bytes per
+        // instruction on the way out), so every global store writes whole
+        // 128-byte lines instead of 16 bytes in each of 32 rows.
         const int q = warp & 3;  // TMEM lanes 32q .. 32q+31
+        float *stg = reinterpret_cast<float *>(smem + (size_t)kStages * kStageBytes + 256) +
+                     (warp - 2) * kStgFloats;
         const uint32_t acce0 = cluster_map(&acce[0], 0);
         int it = 0;
         for (int t = pair; t < nslots; t += npairs, ++it) {
@@ -260,33 +268,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const Slot sl = slot_tile(t, t_full, ntm);
-            const int row = sl.tile_m * PM + (int)rank * BM + q * 32 + lane;
+            const int row0 = sl.tile_m * PM + (int)rank * BM + q * 32;
             const int nchunks = (sl.half ? BNH : BN) / 32;
 #pragma unroll 1
             for (int c = 0; c < nchunks; ++c) {
                 uint32_t r[32];
                 tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c * 32), r);
                 tmem_ld_wait();
-                const int col0 = sl.col0 + c * 32;
-                if (row < Ntok) {
-                    float4 *dst = reinterpret_cast<float4 *>(Y + (int64_t)row * Mw + col0);
+                float4 *srow = reinterpret_cast<float4 *>(stg + lane * kStgStride);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (col0 + 4 * i < Mw) {
-                            float4 v = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                                   __uint_as_float(r[4 * i + 2]),
-                                                   __uint_as_float(r[4 * i + 3]));
-                            if (colscale) {  // per weight row (e.g. HFP4's row_scale_a)
-                                const float4 cs =
-                                    *reinterpret_cast<const float4 *>(colscale + col0 + 4 * i);
-                                v.x *= cs.x;
-                                v.y *= cs.y;
-                                v.z *= cs.z;
-                                v.w *= cs.w;
-                            }
-                            dst[i] = v;
-                        }
+                for (int i = 0; i < 8; ++i)
+                    srow[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                          __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                __syncwarp();
+                const int col = sl.col0 + c * 32 + (lane & 7) * 4;
+                float4 cs = make_float4(1.f, 1.f, 1.f, 1.f);
+                if (colscale && col < Mw)  // per weight row (e.g. HFP4's row_scale_a)
+                    cs = *reinterpret_cast<const float4 *>(colscale + col);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int rr = 4 * j + (lane >> 3);
+                    float4 v = *reinterpret_cast<const float4 *>(stg + rr * kStgStride + (lane & 7) * 4);
+                    if (colscale) {
+                        v.x *= cs.x;
+                        v.y *= cs.y;
+                        v.z *= cs.z;
+                        v.w *= cs.w;
+                    }
+                    if (row0 + rr < Ntok && col < Mw)
+                        *reinterpret_cast<float4 *>(Y + (int64_t)(row0 + rr) * Mw + col) = v;
                 }
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();
