@@ -99,6 +99,17 @@ RFP2_DEV void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
+// Orders this thread's earlier generic-proxy writes to shared memory before
+// later async-proxy reads of it (tensor-core operands, bulk copies).
+RFP2_DEV void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// The same with the default (CTA-scope release) semantics, for a producer
+// whose data is handed over by a proxy fence and an mbarrier phase (the
+// cluster-scope release costs about a microsecond per arrival).
+RFP2_DEV void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 // All threads of all CTAs of the cluster.
 RFP2_DEV void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::

@@ -7,15 +7,18 @@
 // power of two, hence exact in bf16) and "04 Measured evidence" (the
 // end-to-end gain of the format comes from prefill, a dense contraction).
 //
-// Two launches:
-//  1. expand: packed 10-byte blocks -> bf16 rows in the workspace (one thread
-//     per 32-weight block, 64 bytes written per block).  The HFP4G32 variant
-//     (hfp4_gemm) expands E2M1 x 2^(e-127) the same way and leaves the f16
-//     row scale to the GEMM's epilogue.
+// rfp2_gemm is one launch: the GEMM decodes the packed blocks itself (warps
+// 6-22 below); hfp4_gemm runs two:
+//  1. expand: HFP4G32 rows -> bf16 rows in the workspace (one thread per
+//     32-weight block, E2M1 x 2^(e-127), 64 bytes written per block); the f16
+//     row scale is left to the GEMM's epilogue.
 //  2. gemm: persistent over CTA pairs (clusters of two SMs), each pair walking
 //     256-token x 256-weight-row tiles.  In each CTA warp 0 loads its 128
 //     tokens and its 128 of the tile's weight rows, K-major 64-element slices
-//     with 2-D TMA (SWIZZLE_128B) into a 6-stage ring; one thread of the even
+//     with 2-D TMA (SWIZZLE_128B) into a 6-stage ring (5 when decoding: the
+//     ROCmFP2 boxes, 128 rows x 80 bytes = 256 K, stream into a 4-slot ring
+//     and 16 decode warps write each K slice of B as exact bf16 in the same
+//     swizzled layout, one weight row per thread); one thread of the even
 //     CTA issues tcgen05.mma.cta_group::2 kind::f16 (M=256, N=256, K=16, bf16
 //     in, fp32 accumulate) over both CTAs' stages, so each SM stores and reads
 //     only half of the B operand; its commits free the stages of both CTAs and
@@ -45,16 +48,35 @@ constexpr int PM = 256;  // tokens per CTA pair (UMMA M)
 constexpr int BN = 256;  // weight rows per tile (UMMA N), half of them loaded by each CTA
 constexpr int BK = 64;   // K per stage: one 128-byte swizzle row
 constexpr int UK = 16;   // K per UMMA instruction
-constexpr int kStages = 6;
 constexpr int kABytes = BM * BK * 2;
 constexpr int kBBytes = (BN / 2) * BK * 2;  // this CTA's half of the B operand
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 6 * 32;
 constexpr uint32_t kTmemCols = 512;  // two 256-column accumulators
 constexpr int kStgStride = 36;  // floats per row of an epilogue warp's 32 x 32 staging tile
 constexpr int kStgFloats = 32 * kStgStride;
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256 + 4 * kStgFloats * 4;
 constexpr int BNH = BN / 2;  // weight rows of a half tile
+// Packed ROCmFP2 weights decoded inside the GEMM: 128 rows x 80 bytes (eight
+// 10-byte blocks = 256 K) per TMA box, one box per four K slices.
+constexpr int kPBoxRowBytes = 80;
+constexpr int kPBoxBytes = (BN / 2) * kPBoxRowBytes;
+constexpr int kDecodeGroups = 4;         // group i decodes K slices i, i+4, ... (one per box)
+constexpr int kDecodeGroupWarps = 4;     // 512 half-blocks of 16 weights per slice: 4 per thread
+constexpr int kDecodeWarps = kDecodeGroups * kDecodeGroupWarps;
+
+// Per B source: bf16 weights by TMA (kDecode false), or packed ROCmFP2 blocks
+// decoded by kDecodeWarps warps into the B stages (kDecode true).
+template <bool kDecode>
+struct GemmCfg {
+    static constexpr int kStages = kDecode ? 5 : 6;
+    static constexpr int kPStages = kDecode ? 4 : 0;
+    // warps: 0 A (and B) loads, 1 MMA, 2-5 epilogue; kDecode: 6 packed-box
+    // loads, 7.. decode
+    static constexpr int kThreads = (6 + (kDecode ? 1 + kDecodeWarps : 0)) * 32;
+    static constexpr size_t kPRingOff = (size_t)kStages * kStageBytes;
+    static constexpr size_t kBarOff = kPRingOff + (size_t)kPStages * kPBoxBytes;
+    static constexpr size_t kStgOff = kBarOff + 256;
+    static constexpr size_t kSmemBytes = 1024 + kStgOff + 4 * kStgFloats * 4;
+};
 
 // ---- expand ----------------------------------------------------------------
 // OCP E2M1 code -> float: magnitude index k = c & 7 is 0 (0), 1 (0.5) or,
@@ -144,18 +166,30 @@ __device__ __forceinline__ Slot slot_tile(int t, int t_full, int ntm) {
 // copies complete on it), empty[s] and accf[b] (both CTAs; pair commits
 // arrive on both), acce[b] (even CTA; the eight epilogue warps of the pair).
 // colscale[m]: optional per-weight-row factor applied to every output.
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+//
+// kDecode: wmap is unused and wmap_h maps the packed ROCmFP2 weights (bytes,
+// box 80 x 128 rows); warp 6 streams those boxes into a 4-slot ring, running
+// up to four boxes ahead of the decode, and warps 7.. decode each K slice of their CTA's B half (a thread takes 16-weight
+// halves of consecutive rows) exactly to bf16, store it in the SWIZZLE_128B
+// layout the TMA would have written, and arrive on the even CTA's full barrier.
+template <bool kDecode>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<kDecode>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                 const __grid_constant__ CUtensorMap wmap_h, float *__restrict__ Y, int Ntok, int Mw,
                 int K, int t_full, const float *__restrict__ colscale, int32_t *status) {
+    using Cfg = GemmCfg<kDecode>;
+    constexpr int kStages = Cfg::kStages, kPStages = Cfg::kPStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kStages * kStageBytes);
+    uint8_t *pring = smem + Cfg::kPRingOff;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::kBarOff);
     uint64_t *empty = full + kStages;
     uint64_t *accf = empty + kStages;  // [2] accumulator b complete
     uint64_t *acce = accf + 2;         // [2] accumulator b read back (even CTA)
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acce + 2);
+    uint64_t *pfull = acce + 2;        // [kPStages] packed box landed
+    uint64_t *pempty = pfull + kPStages;  // [kPStages] packed box decoded
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(pempty + kPStages);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -171,12 +205,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         prefetch_tensor_map(&wmap);
         prefetch_tensor_map(&wmap_h);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
+            // the producer's arrival (+ every decode warp of the pair)
+            mbar_init(&full[s], kDecode ? 1 + 2 * kDecodeGroupWarps : 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf[b], 1);
             mbar_init(&acce[b], 8);  // one arrival per epilogue warp of the pair
+        }
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(&pfull[s], 1);
+            mbar_init(&pempty[s], kDecodeWarps);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -193,7 +232,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int g = 0;  // k-blocks loaded by this CTA (producer thread)
     if (warp == 0 && lane == 0) {
         // ---- TMA producer (both CTAs)
-        pdl_wait();  // X and the expanded weights come from earlier kernels
+        pdl_wait();  // X (and the expanded weights) may come from earlier kernels
         const uint32_t full0 = cluster_map(&full[0], 0);
         for (int t = pair; t < nslots && !*abort_flag; t += npairs) {
             const Slot sl = slot_tile(t, t_full, ntm);
@@ -208,9 +247,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (*abort_flag) break;
                 uint8_t *a = smem + (size_t)s * kStageBytes;
-                if (rank == 0) mbar_arrive_expect_tx(&full[s], 2u * (uint32_t)(kABytes + brows * BK * 2));
-                tma_load_2d_pair(a, &xmap, kb * BK, arow, full0 + 8u * s);
-                tma_load_2d_pair(a + kABytes, sl.half ? &wmap_h : &wmap, kb * BK, brow, full0 + 8u * s);
+                if (kDecode) {
+                    if (rank == 0) mbar_arrive_expect_tx(&full[s], 2u * (uint32_t)kABytes);
+                    tma_load_2d_pair(a, &xmap, kb * BK, arow, full0 + 8u * s);
+                } else {
+                    if (rank == 0)
+                        mbar_arrive_expect_tx(&full[s], 2u * (uint32_t)(kABytes + brows * BK * 2));
+                    tma_load_2d_pair(a, &xmap, kb * BK, arow, full0 + 8u * s);
+                    tma_load_2d_pair(a + kABytes, sl.half ? &wmap_h : &wmap, kb * BK, brow,
+                                     full0 + 8u * s);
+                }
             }
         }
     } else if (warp == 1 && rank == 0 && lane == 0) {
@@ -248,15 +294,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             umma_commit_pair_both(&accf[b]);  // accumulator complete (or, after an abort, idle)
         }
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < 6) {
         // ---- epilogue (both CTAs): TMEM -> registers -> Y, one tile behind the MMAs.
         // Each 32-row x 32-column chunk goes through a padded shared-memory
         // tile (row = lane on the way in, four rows of 128 bytes per
         // instruction on the way out), so every global store writes whole
         // 128-byte lines instead of 16 bytes in each of 32 rows.
         const int q = warp & 3;  // TMEM lanes 32q .. 32q+31
-        float *stg = reinterpret_cast<float *>(smem + (size_t)kStages * kStageBytes + 256) +
-                     (warp - 2) * kStgFloats;
+        float *stg = reinterpret_cast<float *>(smem + Cfg::kStgOff) + (warp - 2) * kStgFloats;
         const uint32_t acce0 = cluster_map(&acce[0], 0);
         int it = 0;
         for (int t = pair; t < nslots; t += npairs, ++it) {
@@ -305,6 +350,96 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive_cluster(acce0 + 8u * b);
         }
     }
+    if constexpr (kDecode) {
+        if (warp == 6 && lane == 0) {
+            // ---- packed-box producer (both CTAs): the rows of this CTA's B half,
+            // 256 K per box, in the decoders' order
+            pdl_wait();  // W may come from an earlier kernel
+            int u = 0;
+            bool ok = true;
+            for (int t = pair; t < nslots && ok; t += npairs) {
+                const Slot sl = slot_tile(t, t_full, ntm);
+                const int brow = sl.col0 + (int)rank * (sl.half ? BNH / 2 : BN / 2);
+                for (int kq = 0; kq < nk / 4; ++kq, ++u) {
+                    const int ps = u % kPStages;
+                    if (*abort_flag ||
+                        (u >= kPStages && !mbar_wait(&pempty[ps], ((u / kPStages) - 1) & 1))) {
+                        record_status(status, RFP2_ETIMEOUT);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&pfull[ps], kPBoxBytes);
+                    tma_load_2d(pring + (size_t)ps * kPBoxBytes, &wmap_h, kq * kPBoxRowBytes, brow,
+                                &pfull[ps]);
+                }
+            }
+            // boxes still in flight must land before the CTA retires
+            for (int i = max(0, u - kPStages); i < u; ++i)
+                if (!mbar_wait(&pfull[i % kPStages], (i / kPStages) & 1))
+                    record_status(status, RFP2_ETIMEOUT);
+        } else if (warp >= 7) {
+            // ---- decoders (both CTAs).  Group gi takes K slices gi, gi + 4, ...
+            // of every tile (slice gi of each packed box), so the groups' waits
+            // and arrivals overlap; thread tig decodes row tig of this CTA's B
+            // half: two 10-byte blocks at byte 20 gi of its 80-byte box row,
+            // read as two 16-byte words (conflict-free: rows are 80 bytes apart).
+            static_assert(kDecodeGroupWarps * 32 == BN / 2, "one B row per decode thread");
+            const int gi = (warp - 7) / kDecodeGroupWarps;
+            const int row = ((warp - 7) % kDecodeGroupWarps) * 32 + lane;
+            const int wq = (20 * gi & 15) >> 2;  // first word of the slice in the 32-byte window
+            const uint32_t full0 = cluster_map(&full[0], 0);
+            int gbase = 0, ud = 0;  // k-blocks of earlier tiles, boxes decoded
+            bool ok = true;
+            for (int t = pair; t < nslots && ok; t += npairs, gbase += nk) {
+                const bool active = row < (t >= t_full ? BNH / 2 : BN / 2);
+                for (int kb = gi; kb < nk; kb += kDecodeGroups, ++ud) {
+                    const int gd = gbase + kb, s = gd % kStages, ps = ud % kPStages;
+                    bool w_ok = !*abort_flag && mbar_wait(&pfull[ps], (ud / kPStages) & 1);
+                    if (gd >= kStages) w_ok = w_ok && mbar_wait(&empty[s], ((gd / kStages) - 1) & 1);
+                    if (!__all_sync(0xffffffffu, w_ok)) {
+                        if (lane == 0) record_status(status, RFP2_ETIMEOUT);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    if (active) {
+                        const uint4 *win = reinterpret_cast<const uint4 *>(
+                            pring + (size_t)ps * kPBoxBytes + row * kPBoxRowBytes + ((20 * gi) & ~15));
+                        const uint4 q0 = win[0], q1 = win[1];
+                        const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                        uint32_t w[5];
+#pragma unroll
+                        for (int i = 0; i < 5; ++i)  // wq is warp-uniform: a select, not a local array
+                            w[i] = wq == 0 ? wv[i] : wq == 1 ? wv[i + 1] : wq == 2 ? wv[i + 2] : wv[i + 3];
+                        // block 0: codes w0, w1, scales in the low half of w2;
+                        // block 1: codes bytes 10-17, scales in the high half of w4
+                        const uint32_t code[4] = {w[0], w[1], __funnelshift_r(w[2], w[3], 16),
+                                                  __funnelshift_r(w[3], w[4], 16)};
+                        float sc[4];
+                        decode_scale_pair(w[2] & 0xFFFFu, sc[0], sc[1]);
+                        decode_scale_pair(w[4] >> 16, sc[2], sc[3]);
+                        uint8_t *brow_s = smem + (size_t)s * kStageBytes + kABytes + row * 128;
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {  // 16 weights = two 16-byte chunks each
+                            uint32_t o[8];
+                            decode_half_bf16(code[h], sc[h], o);
+                            *reinterpret_cast<uint4 *>(brow_s + (((2 * h) ^ (row & 7)) << 4)) =
+                                make_uint4(o[0], o[1], o[2], o[3]);
+                            *reinterpret_cast<uint4 *>(brow_s + (((2 * h + 1) ^ (row & 7)) << 4)) =
+                                make_uint4(o[4], o[5], o[6], o[7]);
+                        }
+                    }
+                    fence_proxy_async_smem();  // the tensor core reads these bytes next
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive_remote(full0 + 8u * s);
+                        mbar_arrive(&pempty[ps]);
+                    }
+                }
+            }
+        }
+    }
     if (warp == 0 && lane == 0) {
         // The pair commits of the last stages arrive on this CTA's empty
         // barriers (and the other CTA's copies on the even CTA's full
@@ -337,20 +472,14 @@ static int64_t gemm_split_point(int64_t ntiles, int pairs) {
     return (rem > 0 && rem <= pairs / 2) ? ntiles - rem : ntiles;
 }
 
-// Tensor maps for one GEMM launch and the launch itself: one CTA pair per
-// pair of SMs that can hold one at a time (as many as the device reports for
-// this kernel's size), or one per slot when there are fewer slots.
-static rfp2_status launch_gemm(const uint16_t *X, const __nv_bfloat16 *wexp, int64_t N, int64_t M,
-                               int64_t K, float *Y, const float *colscale, int32_t *dev_status,
-                               cudaStream_t s) {
-    CUtensorMap xmap, wmap, wmap_h;
-    if (!encode_tensor_map_2d(&xmap, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K, (uint64_t)N,
-                              (uint64_t)K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map_2d(&wmap, wexp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K,
-                              (uint64_t)M, (uint64_t)K * 2, BK, BN / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map_2d(&wmap_h, wexp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K,
-                              (uint64_t)M, (uint64_t)K * 2, BK, BNH / 2, CU_TENSOR_MAP_SWIZZLE_128B))
-        return RFP2_ECUDA;
+// One GEMM launch: one CTA pair per pair of SMs that can hold one at a time
+// (as many as the device reports for this kernel's size), or one per slot
+// when there are fewer slots.  kDecode: wmap_h maps the packed ROCmFP2 rows.
+template <bool kDecode>
+static rfp2_status launch_gemm(const CUtensorMap &xmap, const CUtensorMap &wmap,
+                               const CUtensorMap &wmap_h, int64_t N, int64_t M, int64_t K, float *Y,
+                               const float *colscale, int32_t *dev_status, cudaStream_t s) {
+    using Cfg = GemmCfg<kDecode>;
     static std::mutex mu;
     static int max_pairs[64] = {0};
     const int dev = current_device();
@@ -360,13 +489,14 @@ static rfp2_status launch_gemm(const uint16_t *X, const __nv_bfloat16 *wexp, int
         if (dev < 64 && max_pairs[dev] > 0) {
             pairs = max_pairs[dev];
         } else {
-            if (set_smem_limit(gemm_kernel, (int)kSmemBytes) != cudaSuccess) return RFP2_ECUDA;
+            if (set_smem_limit(gemm_kernel<kDecode>, (int)Cfg::kSmemBytes) != cudaSuccess)
+                return RFP2_ECUDA;
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2);
-            cfg.blockDim = dim3(kThreads);
-            cfg.dynamicSmemBytes = kSmemBytes;
-            if (cudaOccupancyMaxActiveClusters(&pairs, reinterpret_cast<const void *>(gemm_kernel),
-                                               &cfg) != cudaSuccess ||
+            cfg.blockDim = dim3(Cfg::kThreads);
+            cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+            if (cudaOccupancyMaxActiveClusters(
+                    &pairs, reinterpret_cast<const void *>(gemm_kernel<kDecode>), &cfg) != cudaSuccess ||
                 pairs <= 0)
                 return RFP2_ECUDA;
             if (dev < 64) max_pairs[dev] = pairs;
@@ -376,32 +506,40 @@ static rfp2_status launch_gemm(const uint16_t *X, const __nv_bfloat16 *wexp, int
     const int64_t t_full = gemm_split_point(tiles, pairs);
     const int64_t nslots = t_full + 2 * (tiles - t_full);
     const dim3 grid((unsigned)(2 * std::min<int64_t>(nslots, pairs)));
-    return from_cuda(launch(gemm_kernel, grid, dim3(kThreads), kSmemBytes, s, true, xmap, wmap, wmap_h,
-                            Y, (int)N, (int)M, (int)K, (int)t_full, colscale, dev_status));
+    return from_cuda(launch(gemm_kernel<kDecode>, grid, dim3(Cfg::kThreads), Cfg::kSmemBytes, s, true,
+                            xmap, wmap, wmap_h, Y, (int)N, (int)M, (int)K, (int)t_full, colscale,
+                            dev_status));
+}
+
+static bool encode_x_map(CUtensorMap *xmap, const uint16_t *X, int64_t N, int64_t K) {
+    return encode_tensor_map_2d(xmap, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K, (uint64_t)N,
+                                (uint64_t)K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 extern "C" size_t rfp2_gemm_workspace_bytes(int64_t M, int64_t K) {
-    if (M <= 0 || K <= 0) return 0;
-    return (size_t)M * K * 2;
+    (void)M;
+    (void)K;
+    return 0;
 }
 
 extern "C" rfp2_status rfp2_gemm(const uint8_t *W, int64_t M, int64_t K, const uint16_t *X,
                                  int64_t N, float *Y, void *workspace, size_t workspace_bytes,
                                  int32_t *dev_status, rfp2_stream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
     if (!W || !X || !Y) return RFP2_EINVAL;
     if (M <= 0 || K <= 0 || N <= 0) return RFP2_ESHAPE;
     if (M > (1LL << 30) || N > (1LL << 30) || K > (1 << 20)) return RFP2_ESHAPE;
     if (K % 256 != 0 || M % 16 != 0) return RFP2_EUNSUPPORTED;
-    if (!workspace || workspace_bytes < (size_t)M * K * 2) return RFP2_EWORKSPACE;
-    if (!aligned(W, 16) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(workspace, 256))
-        return RFP2_EALIGN;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    __nv_bfloat16 *wexp = static_cast<__nv_bfloat16 *>(workspace);
-    const int64_t nblocks = M * (K / 32);
-    cudaError_t e = launch(expand_kernel<__nv_bfloat16>, dim3((unsigned)((nblocks + 255) / 256)), dim3(256),
-                           0, s, true, W, nblocks, wexp);
-    if (e != cudaSuccess) return RFP2_ECUDA;
-    return launch_gemm(X, wexp, N, M, K, Y, nullptr, dev_status, s);
+    if (!aligned(W, 16) || !aligned(X, 16) || !aligned(Y, 16)) return RFP2_EALIGN;
+    const uint64_t row_bytes = (uint64_t)(K / 32) * 10;  // a multiple of 80
+    CUtensorMap xmap, pmap;
+    if (!encode_x_map(&xmap, X, N, K) ||
+        !encode_tensor_map_2d(&pmap, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, (uint64_t)M,
+                              row_bytes, kPBoxRowBytes, BN / 2, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return RFP2_ECUDA;
+    return launch_gemm<true>(xmap, pmap, pmap, N, M, K, Y, nullptr, dev_status,
+                             reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---- HFP4G32 prefill GEMM ------------------------------------------------------
@@ -435,5 +573,12 @@ extern "C" rfp2_status hfp4_gemm(const uint8_t *W, int64_t M, int64_t K, const u
     cudaError_t e = launch(hfp4_expand_bf16_kernel, dim3((unsigned)((nblocks + 255) / 256)),
                            dim3(256), 0, s, true, W, (int)M, KB, rb, wexp, rs32);
     if (e != cudaSuccess) return RFP2_ECUDA;
-    return launch_gemm(X, wexp, N, M, K, Y, rs32, dev_status, s);
+    CUtensorMap xmap, wmap, wmap_h;
+    if (!encode_x_map(&xmap, X, N, K) ||
+        !encode_tensor_map_2d(&wmap, wexp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K,
+                              (uint64_t)M, (uint64_t)K * 2, BK, BN / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_2d(&wmap_h, wexp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K,
+                              (uint64_t)M, (uint64_t)K * 2, BK, BNH / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+        return RFP2_ECUDA;
+    return launch_gemm<false>(xmap, wmap, wmap_h, N, M, K, Y, rs32, dev_status, s);
 }

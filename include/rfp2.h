@@ -172,15 +172,18 @@ rfp2_status rfp2_moe_gemv(const uint8_t *W, int64_t E, int64_t M, int64_t K,
 /* ---------------------------------------------------------------------------
  * Prefill GEMM on the tensor cores ("ROCmFP2 codebook research report",
  * section "04 Measured evidence": the end-to-end gain comes from prefill).
- * Y[n, m] = sum_k X[n, k] * w[m, k], with w = codebook * scale expanded
- * exactly to bf16 (at most 4 significant bits times a power of two) and fp32
- * accumulation in tensor memory.  No activation quantization on this path.
- *   W  uint8 [M, K/32, 10] device.  X bf16 bits [N, K] device, 16-byte
- *   aligned.  Y fp32 [N, M] device (output), 16-byte aligned.
+ * Y[n, m] = sum_k X[n, k] * w[m, k], with w = codebook * scale decoded
+ * exactly to bf16 (at most 4 significant bits times a power of two) inside
+ * the GEMM kernel, straight into the tensor cores' shared-memory operand
+ * stages, and fp32 accumulation in tensor memory.  One launch; no
+ * activation quantization on this path.
+ *   W  uint8 [M, K/32, 10] device, 16-byte aligned.  X bf16 bits [N, K]
+ *   device, 16-byte aligned.  Y fp32 [N, M] device (output), 16-byte aligned.
  *   M % 16 == 0, N >= 1, K % 256 == 0.
- *   workspace: rfp2_gemm_workspace_bytes(M, K) bytes, 256-byte aligned
- *   (holds the expanded bf16 weights [M, K]).
- * Errors: EINVAL, ESHAPE, EUNSUPPORTED, EALIGN, EWORKSPACE, ECUDA.
+ *   workspace: unused (rfp2_gemm_workspace_bytes returns 0; NULL is fine).
+ *   The kernel may start while the previous kernel on the stream is still
+ *   running and reads X and W only after that kernel has completed.
+ * Errors: EINVAL, ESHAPE, EUNSUPPORTED, EALIGN, ECUDA.
  */
 size_t rfp2_gemm_workspace_bytes(int64_t M, int64_t K);
 rfp2_status rfp2_gemm(const uint8_t *W, int64_t M, int64_t K, const uint16_t *X, int64_t N,
