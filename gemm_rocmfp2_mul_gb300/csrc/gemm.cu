@@ -25,10 +25,10 @@
 //     signal both epilogues.  Warps 2-5 of each CTA read that CTA's 128 rows
 //     of the accumulator back with tcgen05.ld and store fp32 rows while the
 //     next tile's MMAs run in the other of two 256-column accumulators.  When
-//     the last wave of whole tiles would leave most pairs idle (at most half
-//     of them busy), its tiles are split into 256 x 128 halves spread over
-//     twice as many pairs.  Every wait is bounded; tensor memory is always
-//     freed.
+//     the last wave of whole tiles would leave most pairs idle, its tiles run
+//     as 256 x 128 halves or 256 x 64 quarters spread over more pairs,
+//     whichever ends the wave sooner.  Every wait is bounded; tensor memory
+//     is always freed.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -139,20 +139,16 @@ __global__ void __launch_bounds__(256) hfp4_expand_bf16_kernel(const uint8_t *__
 // ---- GEMM --------------------------------------------------------------------
 // Schedule slot t -> output tile of a CTA pair.  Slots below t_full are whole
 // 256-token x 256-weight-row tiles (token tile f % ntm of weight tile f / ntm,
-// f = t); each tile after them takes two slots, one per 128-row half of its
-// weight rows.
+// f = t); each tile after them takes 2^split_lg slots, one per part of its
+// weight rows (256 >> split_lg of them).
 struct Slot {
     int tile_m, col0;  // token tile of the pair; first weight row (output column)
-    bool half;
+    int width;         // weight rows (MMA N): 256, 128 or 64
 };
-__device__ __forceinline__ Slot slot_tile(int t, int t_full, int ntm) {
-    int f = t, h = 0;
-    const bool half = t >= t_full;
-    if (half) {
-        f = t_full + ((t - t_full) >> 1);
-        h = (t - t_full) & 1;
-    }
-    return Slot{f % ntm, (f / ntm) * BN + h * BNH, half};
+__device__ __forceinline__ Slot slot_tile(int t, int t_full, int split_lg, int ntm) {
+    if (t < t_full) return Slot{t % ntm, (t / ntm) * BN, BN};
+    const int h = t - t_full, f = t_full + (h >> split_lg), w = BN >> split_lg;
+    return Slot{f % ntm, (f / ntm) * BN + (h & ((1 << split_lg) - 1)) * w, w};
 }
 
 // Persistent over CTA pairs (clusters of two): pair p takes slots p, p + P,
@@ -167,16 +163,18 @@ __device__ __forceinline__ Slot slot_tile(int t, int t_full, int ntm) {
 // arrive on both), acce[b] (even CTA; the eight epilogue warps of the pair).
 // colscale[m]: optional per-weight-row factor applied to every output.
 //
-// kDecode: wmap is unused and wmap_h maps the packed ROCmFP2 weights (bytes,
-// box 80 x 128 rows); warp 6 streams those boxes into a 4-slot ring, running
+// B maps: 128-, 64- and 32-row boxes for whole, half and quarter tiles.
+// kDecode: wmap maps the packed ROCmFP2 weights (bytes, box 80 x 128 rows)
+// and the other two are unused; warp 6 streams those boxes into a 4-slot ring, running
 // up to four boxes ahead of the decode, and warps 7.. decode each K slice of their CTA's B half (a thread takes 16-weight
 // halves of consecutive rows) exactly to bf16, store it in the SWIZZLE_128B
 // layout the TMA would have written, and arrive on the even CTA's full barrier.
 template <bool kDecode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<kDecode>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-                const __grid_constant__ CUtensorMap wmap_h, float *__restrict__ Y, int Ntok, int Mw,
-                int K, int t_full, const float *__restrict__ colscale, int32_t *status) {
+                const __grid_constant__ CUtensorMap wmap_h, const __grid_constant__ CUtensorMap wmap_q,
+                float *__restrict__ Y, int Ntok, int Mw, int K, int t_full, int split_lg,
+                const float *__restrict__ colscale, int32_t *status) {
     using Cfg = GemmCfg<kDecode>;
     constexpr int kStages = Cfg::kStages, kPStages = Cfg::kPStages;
     extern __shared__ uint8_t smem_raw[];
@@ -198,12 +196,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<kDecode>::kT
     const int nk = K / BK;
     const int ntm = (Ntok + PM - 1) / PM, ntn = (Mw + BN - 1) / BN;
     const int ntiles = ntm * ntn;
-    const int nslots = t_full + 2 * (ntiles - t_full);
+    const int nslots = t_full + ((ntiles - t_full) << split_lg);
 
     if (threadIdx.x == 0) {
         prefetch_tensor_map(&xmap);
         prefetch_tensor_map(&wmap);
         prefetch_tensor_map(&wmap_h);
+        prefetch_tensor_map(&wmap_q);
         for (int s = 0; s < kStages; ++s) {
             // the producer's arrival (+ every decode warp of the pair)
             mbar_init(&full[s], kDecode ? 1 + 2 * kDecodeGroupWarps : 1);
@@ -235,8 +234,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<kDecode>::kT
         pdl_wait();  // X (and the expanded weights) may come from earlier kernels
         const uint32_t full0 = cluster_map(&full[0], 0);
         for (int t = pair; t < nslots && !*abort_flag; t += npairs) {
-            const Slot sl = slot_tile(t, t_full, ntm);
-            const int brows = sl.half ? BNH / 2 : BN / 2;
+            const Slot sl = slot_tile(t, t_full, split_lg, ntm);
+            const int brows = sl.width / 2;
             const int arow = sl.tile_m * PM + (int)rank * BM, brow = sl.col0 + (int)rank * brows;
             for (int kb = 0; kb < nk; ++kb, ++g) {
                 const int s = g % kStages;
@@ -254,14 +253,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<kDecode>::kT
                     if (rank == 0)
                         mbar_arrive_expect_tx(&full[s], 2u * (uint32_t)(kABytes + brows * BK * 2));
                     tma_load_2d_pair(a, &xmap, kb * BK, arow, full0 + 8u * s);
-                    tma_load_2d_pair(a + kABytes, sl.half ? &wmap_h : &wmap, kb * BK, brow,
-                                     full0 + 8u * s);
+                    const CUtensorMap *bm = sl.width == BN ? &wmap : sl.width == BNH ? &wmap_h : &wmap_q;
+                    tma_load_2d_pair(a + kABytes, bm, kb * BK, brow, full0 + 8u * s);
                 }
             }
         }
     } else if (warp == 1 && rank == 0 && lane == 0) {
         // ---- MMA issuer (even CTA)
-        constexpr uint32_t idesc_full = idesc_bf16_f32(PM, BN), idesc_half = idesc_bf16_f32(PM, BNH);
         int gm = 0, it = 0;
         bool ok = true;
         for (int t = pair; t < nslots && ok; t += npairs, ++it) {
@@ -272,7 +270,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<kDecode>::kT
                 break;
             }
             tc_fence_after();
-            const uint32_t idesc = t >= t_full ? idesc_half : idesc_full;
+            const uint32_t idesc = idesc_bf16_f32(PM, slot_tile(t, t_full, split_lg, ntm).width);
             const uint32_t d_tmem = tmem + (uint32_t)(b * BN);
             for (int kb = 0; kb < nk; ++kb, ++gm) {
                 const int s = gm % kStages;
@@ -312,9 +310,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<kDecode>::kT
                 break;
             }
             tc_fence_after();
-            const Slot sl = slot_tile(t, t_full, ntm);
+            const Slot sl = slot_tile(t, t_full, split_lg, ntm);
             const int row0 = sl.tile_m * PM + (int)rank * BM + q * 32;
-            const int nchunks = (sl.half ? BNH : BN) / 32;
+            const int nchunks = sl.width / 32;
 #pragma unroll 1
             for (int c = 0; c < nchunks; ++c) {
                 uint32_t r[32];
@@ -358,8 +356,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<kDecode>::kT
             int u = 0;
             bool ok = true;
             for (int t = pair; t < nslots && ok; t += npairs) {
-                const Slot sl = slot_tile(t, t_full, ntm);
-                const int brow = sl.col0 + (int)rank * (sl.half ? BNH / 2 : BN / 2);
+                const Slot sl = slot_tile(t, t_full, split_lg, ntm);
+                const int brow = sl.col0 + (int)rank * (sl.width / 2);
                 for (int kq = 0; kq < nk / 4; ++kq, ++u) {
                     const int ps = u % kPStages;
                     if (*abort_flag ||
@@ -370,7 +368,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<kDecode>::kT
                         break;
                     }
                     mbar_arrive_expect_tx(&pfull[ps], kPBoxBytes);
-                    tma_load_2d(pring + (size_t)ps * kPBoxBytes, &wmap_h, kq * kPBoxRowBytes, brow,
+                    tma_load_2d(pring + (size_t)ps * kPBoxBytes, &wmap, kq * kPBoxRowBytes, brow,
                                 &pfull[ps]);
                 }
             }
@@ -392,7 +390,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<kDecode>::kT
             int gbase = 0, ud = 0;  // k-blocks of earlier tiles, boxes decoded
             bool ok = true;
             for (int t = pair; t < nslots && ok; t += npairs, gbase += nk) {
-                const bool active = row < (t >= t_full ? BNH / 2 : BN / 2);
+                const bool active = row < slot_tile(t, t_full, split_lg, ntm).width / 2;
                 for (int kb = gi; kb < nk; kb += kDecodeGroups, ++ud) {
                     const int gd = gbase + kb, s = gd % kStages, ps = ud % kPStages;
                     bool w_ok = !*abort_flag && mbar_wait(&pfull[ps], (ud / kPStages) & 1);
@@ -465,11 +463,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<kDecode>::kT
 
 using namespace rfp2;
 
-// Whole-tile slots before the split: the last partial wave is split into half
-// tiles when it would occupy at most half of the pairs.
-static int64_t gemm_split_point(int64_t ntiles, int pairs) {
+// The tiles of the last partial wave run in 2^split_lg parts (1, 2 or 4) when
+// that shortens the wave: R tiles in parts of 1/f take ceil(R f / pairs) / f
+// tile times.  Returns the whole-tile slots before them (t_full).
+static int64_t gemm_split(int64_t ntiles, int pairs, int *split_lg) {
     const int64_t rem = ntiles % pairs;
-    return (rem > 0 && rem <= pairs / 2) ? ntiles - rem : ntiles;
+    *split_lg = 0;
+    if (rem == 0) return ntiles;
+    double best = 1.0;  // one tile time with no split
+    for (int lg = 1; lg <= 2; ++lg) {
+        const int64_t f = 1 << lg;
+        const double t = (double)((rem * f + pairs - 1) / pairs) / (double)f;
+        if (t < best) {
+            best = t;
+            *split_lg = lg;
+        }
+    }
+    return *split_lg ? ntiles - rem : ntiles;
 }
 
 // One GEMM launch: one CTA pair per pair of SMs that can hold one at a time
@@ -477,8 +487,9 @@ static int64_t gemm_split_point(int64_t ntiles, int pairs) {
 // when there are fewer slots.  kDecode: wmap_h maps the packed ROCmFP2 rows.
 template <bool kDecode>
 static rfp2_status launch_gemm(const CUtensorMap &xmap, const CUtensorMap &wmap,
-                               const CUtensorMap &wmap_h, int64_t N, int64_t M, int64_t K, float *Y,
-                               const float *colscale, int32_t *dev_status, cudaStream_t s) {
+                               const CUtensorMap &wmap_h, const CUtensorMap &wmap_q, int64_t N,
+                               int64_t M, int64_t K, float *Y, const float *colscale,
+                               int32_t *dev_status, cudaStream_t s) {
     using Cfg = GemmCfg<kDecode>;
     static std::mutex mu;
     static int max_pairs[64] = {0};
@@ -503,12 +514,13 @@ static rfp2_status launch_gemm(const CUtensorMap &xmap, const CUtensorMap &wmap,
         }
     }
     const int64_t tiles = ((N + PM - 1) / PM) * ((M + BN - 1) / BN);
-    const int64_t t_full = gemm_split_point(tiles, pairs);
-    const int64_t nslots = t_full + 2 * (tiles - t_full);
+    int split_lg = 0;
+    const int64_t t_full = gemm_split(tiles, pairs, &split_lg);
+    const int64_t nslots = t_full + ((tiles - t_full) << split_lg);
     const dim3 grid((unsigned)(2 * std::min<int64_t>(nslots, pairs)));
     return from_cuda(launch(gemm_kernel<kDecode>, grid, dim3(Cfg::kThreads), Cfg::kSmemBytes, s, true,
-                            xmap, wmap, wmap_h, Y, (int)N, (int)M, (int)K, (int)t_full, colscale,
-                            dev_status));
+                            xmap, wmap, wmap_h, wmap_q, Y, (int)N, (int)M, (int)K, (int)t_full,
+                            split_lg, colscale, dev_status));
 }
 
 static bool encode_x_map(CUtensorMap *xmap, const uint16_t *X, int64_t N, int64_t K) {
@@ -538,7 +550,7 @@ extern "C" rfp2_status rfp2_gemm(const uint8_t *W, int64_t M, int64_t K, const u
         !encode_tensor_map_2d(&pmap, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, (uint64_t)M,
                               row_bytes, kPBoxRowBytes, BN / 2, CU_TENSOR_MAP_SWIZZLE_NONE))
         return RFP2_ECUDA;
-    return launch_gemm<true>(xmap, pmap, pmap, N, M, K, Y, nullptr, dev_status,
+    return launch_gemm<true>(xmap, pmap, pmap, pmap, N, M, K, Y, nullptr, dev_status,
                              reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -573,12 +585,14 @@ extern "C" rfp2_status hfp4_gemm(const uint8_t *W, int64_t M, int64_t K, const u
     cudaError_t e = launch(hfp4_expand_bf16_kernel, dim3((unsigned)((nblocks + 255) / 256)),
                            dim3(256), 0, s, true, W, (int)M, KB, rb, wexp, rs32);
     if (e != cudaSuccess) return RFP2_ECUDA;
-    CUtensorMap xmap, wmap, wmap_h;
+    CUtensorMap xmap, wmap, wmap_h, wmap_q;
     if (!encode_x_map(&xmap, X, N, K) ||
         !encode_tensor_map_2d(&wmap, wexp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K,
                               (uint64_t)M, (uint64_t)K * 2, BK, BN / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tensor_map_2d(&wmap_h, wexp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K,
-                              (uint64_t)M, (uint64_t)K * 2, BK, BNH / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+                              (uint64_t)M, (uint64_t)K * 2, BK, BN / 4, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_2d(&wmap_q, wexp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)K,
+                              (uint64_t)M, (uint64_t)K * 2, BK, BN / 8, CU_TENSOR_MAP_SWIZZLE_128B))
         return RFP2_ECUDA;
-    return launch_gemm<false>(xmap, wmap, wmap_h, N, M, K, Y, rs32, dev_status, s);
+    return launch_gemm<false>(xmap, wmap, wmap_h, wmap_q, N, M, K, Y, rs32, dev_status, s);
 }

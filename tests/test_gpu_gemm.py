@@ -58,7 +58,7 @@ def test_gemm_decoded_weights_exact(g, M, K):
     = w[m, k] with a single exact product per output, so Y equals the
     oracle's decoded weights bit for bit (both CTAs of a pair, every 16-byte
     chunk of the 128-byte swizzle rows, all four K slices of a packed box;
-    512 x 512 runs as half tiles only, 2560 x 1024 as 40 whole tiles)."""
+    512 x 512 runs as quarter tiles only, 2560 x 1024 as 40 whole tiles)."""
     W = normal_weights(child_rngs(11, 1)[0], M, K, 0.015)
     P = oracle.rfp2_pack(W)
     X = np.zeros((K, K), np.uint16)
@@ -69,9 +69,10 @@ def test_gemm_decoded_weights_exact(g, M, K):
 
 @pytest.mark.parametrize("M,K,N", [
     (512, 1024, 256), (272, 768, 200), (1024, 2048, 130), (256, 5120, 7), (4096, 512, 1000),
-    # 90 tiles of 256 tokens x 256 weight rows: those past the first wave of
-    # CTA pairs run as half tiles, the last weight tile (16 valid rows) among them
-    (4368, 256, 1100),
+    # 90 tiles of 256 tokens x 256 weight rows: the 14 past the first wave of
+    # 76 CTA pairs run as quarter tiles (N = 64), the last weight tile (16 valid
+    # rows) among them; 30 tiles: all as half tiles (N = 128)
+    (4368, 256, 1100), (2560, 256, 768),
 ])
 def test_gemm_parity(g, M, K, N):
     Y, P, X = _case(g, M, K, N, seed=M + N + K)

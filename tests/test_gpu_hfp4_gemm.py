@@ -64,9 +64,10 @@ def test_hfp4_gemm_single_tile(g):
 
 @pytest.mark.parametrize("M,K,N", [
     (512, 1024, 256), (272, 768, 200), (1024, 2048, 130), (256, 5120, 7), (4096, 512, 1000),
-    # 90 tiles of 256 tokens x 256 weight rows: those past the first wave of
-    # CTA pairs run as half tiles, the last weight tile (16 valid rows) among them
-    (4368, 256, 1100),
+    # 90 tiles of 256 tokens x 256 weight rows: the 14 past the first wave of
+    # 76 CTA pairs run as quarter tiles (N = 64), the last weight tile (16 valid
+    # rows) among them; 30 tiles: all as half tiles (N = 128)
+    (4368, 256, 1100), (2560, 256, 768),
 ])
 def test_hfp4_gemm_parity(g, M, K, N):
     Y, P, X, _ = _case(g, M, K, N, seed=M + N + K)
