@@ -457,8 +457,8 @@ def _sec_gemm(torch, gl, peaks, hfp4=False, reps=3):
         yus = _graph_us(torch, lambda i: torch.matmul(Xb, Wexp.t(), out=Yb), 20, reps)
         yardstick = {"cublas_bf16_us": round(yus, 1),
                      "cublas_bf16_tflops": round(2.0 * M * K * N / yus / 1e6, 1),
-                     "what": "torch.matmul (cuBLAS) bf16 x bf16 -> bf16 on the pre-expanded "
-                             "weights, expansion excluded"}
+                     "what": "torch.matmul (cuBLAS) bf16 x bf16 -> bf16 on bf16 weights of "
+                             "the same shape and spread, no decode"}
         del Wexp, Xb, Yb
     del P, X, Y, ws
     torch.cuda.empty_cache()
