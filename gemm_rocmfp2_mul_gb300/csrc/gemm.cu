@@ -60,7 +60,7 @@ constexpr int BNH = BN / 2;  // weight rows of a half tile
 constexpr int kPBoxRowBytes = 80;
 constexpr int kPBoxBytes = (BN / 2) * kPBoxRowBytes;
 constexpr int kDecodeGroups = 4;         // group i decodes K slices i, i+4, ... (one per box)
-constexpr int kDecodeGroupWarps = 4;     // 512 half-blocks of 16 weights per slice: 4 per thread
+constexpr int kDecodeGroupWarps = 4;     // 128 B rows per slice: one per thread
 constexpr int kDecodeWarps = kDecodeGroups * kDecodeGroupWarps;
 
 // Per B source: bf16 weights by TMA (kDecode false), or packed ROCmFP2 blocks
@@ -154,8 +154,8 @@ __device__ __forceinline__ Slot slot_tile(int t, int t_full, int split_lg, int n
 // Persistent over CTA pairs (clusters of two): pair p takes slots p, p + P,
 // p + 2P, ...  CTA r of the pair loads tokens [256 tm + 128 r, +128) and
 // weight rows [col0 + r n/2, +n/2) of each K slice into its own ring; the even
-// CTA's MMA thread issues M = 256, N = n (256, or 128 for a half tile) pair
-// MMAs over both CTAs' stages, so each SM reads and stores only its half of
+// CTA's MMA thread issues M = 256, N = n (256, or 128 / 64 for the parts of a
+// split tile) pair MMAs over both CTAs' stages, so each SM reads and stores only its half of
 // the B operand.  D rows of CTA r's tokens land in CTA r's tensor memory,
 // alternating between two 256-column accumulators so the epilogue of one tile
 // overlaps the MMAs of the next.  Barriers: full[s] (even CTA; both CTAs'
@@ -165,10 +165,12 @@ __device__ __forceinline__ Slot slot_tile(int t, int t_full, int split_lg, int n
 //
 // B maps: 128-, 64- and 32-row boxes for whole, half and quarter tiles.
 // kDecode: wmap maps the packed ROCmFP2 weights (bytes, box 80 x 128 rows)
-// and the other two are unused; warp 6 streams those boxes into a 4-slot ring, running
-// up to four boxes ahead of the decode, and warps 7.. decode each K slice of their CTA's B half (a thread takes 16-weight
-// halves of consecutive rows) exactly to bf16, store it in the SWIZZLE_128B
-// layout the TMA would have written, and arrive on the even CTA's full barrier.
+// and the other two are unused; warp 6 streams those boxes into a 4-slot
+// ring, up to four boxes ahead of the decode, and warps 7-22 (four groups of
+// four, group i taking K slice i of every box, one weight row of this CTA's
+// B half per thread) decode each slice exactly to bf16, store it in the
+// SWIZZLE_128B layout the TMA would have written, and arrive on the even
+// CTA's full barrier.
 template <bool kDecode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<kDecode>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
