@@ -65,11 +65,27 @@ constexpr int kMaxPStages = 8;
 // columns: three steps of slots at BNT = 32, two at BNT = 64.  The ring depth
 // hides the tensor-memory store of a slot, which competes with the MMAs for
 // tensor memory and waits for the MMAs that last read the slot.
+// At BNT = 128 one accumulator (2*BNT = 256 columns) takes every k-step and
+// the steps are two stages (an activation stage is 32 KB); below, two
+// accumulators take alternate k-steps and the steps are four stages.
 template <int BNT>
-constexpr int vb_aslots() { return (512 - 4 * BNT) / 32 / 4 * 4; }
+constexpr int vb_accs() { return BNT >= 128 ? 1 : 2; }
+template <int BNT>
+constexpr int vb_vq() { return BNT >= 128 ? 2 : 4; }  // MMA stages per step of the issuing warp
+// MMA stages between two read-backs: at most 128 MMAs per accumulator
+template <int BNT>
+constexpr int vb_vround() { return 32 * vb_accs<BNT>(); }
+template <int BNT>
+constexpr int vb_bstages();
+// A slots: what tensor memory leaves beside the accumulators, at most as many
+// steps as the step barriers' ring holds (a slot is reused after the MMAs of
+// the step that last read it, whose barrier must still be in the ring)
+template <int BNT>
+constexpr int vb_aslots() {
+    return std::min((512 - vb_accs<BNT>() * 2 * BNT) / 32 / vb_vq<BNT>() * vb_vq<BNT>(),
+                    vb_bstages<BNT>());
+}
 constexpr int kTmemCols = 512;
-constexpr int VROUND = 64;                  // MMA stages between two read-backs of the accumulators
-constexpr int VQ = 4;                       // MMA stages per step of the issuing warp (one packed stage)
 constexpr int kDecodeWarps = 16;
 constexpr int kGroups = kDecodeWarps / 4;   // decode groups (one warp per TMEM lane quarter)
 constexpr int VTHREADS = (4 + kDecodeWarps) * 32;  // 0 B loads, 1 MMA, 2 W loads, 3 idle, 4.. decode
@@ -80,7 +96,7 @@ constexpr int VTHREADS = (4 + kDecodeWarps) * 32;  // 0 B loads, 1 MMA, 2 W load
 // step's activation tile arrives as one TMA box: the copy engine keeps few
 // boxes in flight, so its throughput grows with the box.
 template <int BNT>
-constexpr int vb_bstages() { return 3 * VQ; }
+constexpr int vb_bstages() { return 3 * vb_vq<BNT>(); }
 // mbarriers (2 per activation stage, 2 per packed stage, 2 per A slot, 3
 // more), the TMEM address and the abort flag
 constexpr int kVbBarrierBytes = 1024;
@@ -251,14 +267,16 @@ __global__ void __launch_bounds__(VTHREADS, 1)
     vb_fused_kernel(const __grid_constant__ CUtensorMap pmap, const __grid_constant__ CUtensorMap xmap,
                     float *__restrict__ y, int Mw, int Ntok, int K, const int *__restrict__ kc,
                     int32_t *status) {
+    constexpr int VQ = vb_vq<BNT>(), VROUND = vb_vround<BNT>(), NACC = vb_accs<BNT>();
     constexpr int SB = vb_bstages<BNT>();
     constexpr int BB = vb_bstage_bytes<BNT>();
     constexpr int QS = SB / VQ;  // step barriers
     constexpr int VPSTAGES = vb_pstages<BNT>();
     constexpr int kASlots = vb_aslots<BNT>();
-    constexpr int kACol0 = 4 * BNT;
+    constexpr int kACol0 = NACC * 2 * BNT;
     constexpr int AQ = kASlots / VQ;  // steps of lookahead in the A ring
     static_assert(SB % VQ == 0 && kASlots % VQ == 0 && AQ >= 2 && QS >= 3, "step rings");
+    static_assert(AQ <= QS, "A-slot lookahead within the ring of step barriers");
     static_assert(kACol0 + 32 * kASlots <= kTmemCols, "tensor memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -289,7 +307,8 @@ __global__ void __launch_bounds__(VTHREADS, 1)
         prefetch_tensor_map(&pmap);
         prefetch_tensor_map(&xmap);
         for (int s = 0; s < QS; ++s) {
-            mbar_init(&fullq[s], 1 + kDecodeWarps);  // the TMA producer, every decode warp
+            // the TMA producer and the decode warps of the step's VQ stages
+            mbar_init(&fullq[s], 1 + VQ * (kDecodeWarps / kGroups));
             mbar_init(&emptyq[s], 1);
         }
         for (int s = 0; s < VPSTAGES; ++s) {
@@ -385,9 +404,9 @@ __global__ void __launch_bounds__(VTHREADS, 1)
                     const uint64_t bdesc = bdesc0 + (uint64_t)(((t % SB) * BB) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < VSTEP / VUK; ++kk)
-                        umma_f16_tmem_a(tmem + (uint32_t)((kk & 1) * NB), a_tmem + 8 * kk,
+                        umma_f16_tmem_a(tmem + (uint32_t)((kk % NACC) * NB), a_tmem + 8 * kk,
                                         bdesc + 2 * kk, idesc,
-                                        (fresh && st == 0 && kk < 2) ? 0u : 1u);
+                                        (fresh && st == 0 && kk < NACC) ? 0u : 1u);
                 }
                 umma_commit(&emptyq[qs]);  // frees the step's B stages and A slots
                 if (((u + 1) * VQ) % VROUND == 0 || u == NQ - 1) umma_commit(accf);
@@ -416,16 +435,21 @@ __global__ void __launch_bounds__(VTHREADS, 1)
                 return false;
             }
             tc_fence_after();
+            constexpr int TC = TQ < 16 ? TQ : 16;  // columns per read
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
+            for (int j = 0; j < NACC; ++j)
 #pragma unroll
-                for (int piece = 0; piece < 2; ++piece) {
-                    uint32_t v[TQ];
-                    tmem_ld_cols<TQ>(lane_base + tmem + (uint32_t)(j * NB + piece * BNT + g * TQ), v);
-                    tmem_ld_wait();
+                for (int piece = 0; piece < 2; ++piece)
 #pragma unroll
-                    for (int i = 0; i < TQ; ++i) acc[i] += __uint_as_float(v[i]);
-                }
+                    for (int c0 = 0; c0 < TQ; c0 += TC) {
+                        uint32_t v[TC];
+                        tmem_ld_cols<TC>(lane_base + tmem +
+                                             (uint32_t)(j * NB + piece * BNT + g * TQ + c0),
+                                         v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < TC; ++i) acc[c0 + i] += __uint_as_float(v[i]);
+                    }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce);
@@ -498,7 +522,7 @@ struct VbWs {
     size_t bytes;
 };
 
-int64_t vb_bnt(int64_t N) { return N <= 32 ? 32 : 64; }
+int64_t vb_bnt(int64_t N) { return N <= 32 ? 32 : N <= 64 ? 64 : 128; }
 int64_t vb_tiles_n(int64_t N) { return (N + vb_bnt(N) - 1) / vb_bnt(N); }
 
 VbWs carve_vb(void *ws, int64_t M, int64_t K, int64_t N) {
@@ -528,7 +552,7 @@ cudaError_t launch_vb_fused(const uint8_t *W, const VbWs &w, float *y, int64_t M
     // the tile's 2*BNT rows, laid out as VQ consecutive SWIZZLE_128B tiles
     const uint64_t xdims[3] = {(uint64_t)VSTEP, xrows, (uint64_t)(K / VSTEP)};
     const uint64_t xstrides[2] = {(uint64_t)K * 2, (uint64_t)VSTEP * 2};
-    const uint32_t xbox[3] = {(uint32_t)VSTEP, (uint32_t)(2 * BNT), (uint32_t)VQ};
+    const uint32_t xbox[3] = {(uint32_t)VSTEP, (uint32_t)(2 * BNT), (uint32_t)vb_vq<BNT>()};
     if (!encode_tensor_map_2d(&pmap, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, row_bytes, (uint64_t)M,
                               row_bytes, kPRowBytes, VBM) ||
         !encode_tensor_map_3d(&xmap, w.xp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xdims, xstrides, xbox,
@@ -577,6 +601,7 @@ extern "C" rfp2_status rfp2_gemv_batched(const uint8_t *W, int64_t M, int64_t K,
                            (int)vb_bnt(N), w.q, w.d, w.xp, w.kc);
     if (e != cudaSuccess) return RFP2_ECUDA;
     if (N <= 32) e = launch_vb_fused<32>(W, w, y, M, K, N, dev_status, s);
-    else e = launch_vb_fused<64>(W, w, y, M, K, N, dev_status, s);
+    else if (N <= 64) e = launch_vb_fused<64>(W, w, y, M, K, N, dev_status, s);
+    else e = launch_vb_fused<128>(W, w, y, M, K, N, dev_status, s);
     return from_cuda(e);
 }

@@ -45,6 +45,7 @@ def _ws_qd(wsh, M, K, N):
 @pytest.mark.parametrize("M,K,N", [
     (256, 1024, 32), (512, 4096, 128), (272, 2048, 37), (1024, 768, 200), (128, 512, 1),
     (256, 8192, 40), (144, 16384, 5),  # several read-backs of the accumulators along K
+    (128, 16384, 100),  # a 128-token tile: one accumulator, eight read-backs
 ])
 def test_verify_batch_parity(g, M, K, N):
     import torch
