@@ -31,12 +31,14 @@
 //       2*BNT rows, SWIZZLE_128B);
 //     - warp 1 issues tcgen05.mma kind::f16 (A in TMEM, B in shared memory;
 //       M = 128 weight rows, N = 2*BNT = the tokens' hi and lo pieces, K =
-//       16, fp32 in TMEM), the k-steps alternating between two accumulators.
-//       The tensor cores' fp32 accumulation does not round to nearest (over
-//       K = 4096 in one accumulator ~1.5e-5 relative), so no accumulator
-//       takes more than 128 MMAs before the decode warps add it into fp32
-//       registers (one weight row and a quarter of the tokens per thread,
-//       hi + lo; every 64 stages) and, at the end, store y with 2^kc.
+//       16, fp32 in TMEM); at BNT = 32 and 64 the k-steps alternate between
+//       two accumulators, at BNT = 128 (65 tokens and up) one 256-column
+//       accumulator takes them all.  The tensor cores' fp32 accumulation
+//       does not round to nearest (over K = 4096 in one accumulator ~1.5e-5
+//       relative), so no accumulator takes more than 128 MMAs before the
+//       decode warps add it into fp32 registers (one weight row and a
+//       quarter of the tokens per thread, hi + lo; every 64 stages with two
+//       accumulators, 32 with one) and, at the end, store y with 2^kc.
 #include <algorithm>
 #include <mutex>
 
@@ -60,11 +62,12 @@ constexpr int kPStageBytes = VBM * kPRowBytes;
 template <int BNT>
 constexpr int vb_pstages() { return BNT <= 32 ? 8 : 3; }
 constexpr int kMaxPStages = 8;
-// TMEM: the two accumulators (2 x 2*BNT fp32 columns), then the A ring of
-// 32-column slots (64 f16 values of 128 rows) in what is left of the 512
-// columns: three steps of slots at BNT = 32, two at BNT = 64.  The ring depth
-// hides the tensor-memory store of a slot, which competes with the MMAs for
-// tensor memory and waits for the MMAs that last read the slot.
+// TMEM: the accumulators (2 x 2*BNT fp32 columns, or 1 x 256 at BNT = 128),
+// then the A ring of 32-column slots (64 f16 values of 128 rows) in what is
+// left of the 512 columns: three steps of slots at BNT = 32, two at BNT = 64,
+// three (of two stages) at BNT = 128.  The ring depth hides the
+// tensor-memory store of a slot, which competes with the MMAs for tensor
+// memory and waits for the MMAs that last read the slot.
 // At BNT = 128 one accumulator (2*BNT = 256 columns) takes every k-step and
 // the steps are two stages (an activation stage is 32 KB); below, two
 // accumulators take alternate k-steps and the steps are four stages.
