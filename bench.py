@@ -501,7 +501,34 @@ def _sec_verify(torch, gl, peaks, reps=3):
     return out
 
 
+def _sec_decode(torch, gl, peaks, N=1, reps=3):
+    """The decode GEMV alone (batch N through rfp2_gemv), the headline
+    workload's kernel in a graph of back-to-back calls over rotating copies."""
+    from synth import decode_gemv
+    w = decode_gemv(N=max(N, 1))
+    P = gl.rfp2_pack_weights(torch.from_numpy(w["W"]).cuda())
+    torch.cuda.synchronize()
+    copies = max(4, -(-4 * L2_BYTES // WEIGHT_BYTES))
+    copies = 1 << (copies - 1).bit_length()
+    Pc = torch.empty((copies,) + tuple(P.shape), dtype=torch.uint8, device="cuda")
+    Pc[:] = P
+    x = torch.from_numpy(w["x"][:N].copy()).cuda()
+    y = torch.empty((N, M_DEC), dtype=torch.float32, device="cuda")
+    ws = torch.empty(gl.rfp2_gemv_workspace_bytes(N, K_DEC), dtype=torch.uint8, device="cuda")
+    us = _graph_us(torch, lambda i: gl.rfp2_gemv(Pc[i % copies], M_DEC, K_DEC, x, y=y,
+                                                 workspace=ws), 200, reps)
+    del P, Pc
+    torch.cuda.empty_cache()
+    return {f"decode_batch{N}_alone": {
+        "workload": f"ROCmFP2 decode weights [14336, 4096] (seed 1), batch {N}; {copies} copies rotate",
+        "value": round(WEIGHT_BYTES / us / 1e3, 1), "unit": "GB/s (packed bytes)",
+        "us_per_call": round(us, 3),
+        "frac_of_hbm_peak": round(WEIGHT_BYTES / us / 1e3 / peaks["hbm_gbs"], 4)}}
+
+
 SECONDARY_ROWS = {
+    "decode1": lambda torch, gl, peaks, reps=3: _sec_decode(torch, gl, peaks, 1, reps),
+    "decode4": lambda torch, gl, peaks, reps=3: _sec_decode(torch, gl, peaks, 4, reps),
     "verify": _sec_verify,
     "moe": _sec_moe,
     "hfp4": _sec_hfp4,
@@ -514,8 +541,9 @@ def secondary(torch, gl, peaks):
     """The other rows of the hot path, each on its own synthetic workload, in
     CUDA graphs of back-to-back calls over weight copies larger than L2."""
     out = {}
-    for fn in SECONDARY_ROWS.values():
-        out.update(fn(torch, gl, peaks))
+    for name, fn in SECONDARY_ROWS.items():
+        if not name.startswith("decode"):
+            out.update(fn(torch, gl, peaks))
     return out
 
 

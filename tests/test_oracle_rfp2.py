@@ -426,3 +426,66 @@ def test_weighted_pack_never_loses_on_its_own_objective():
                 assert ew <= ep
                 better += ew < ep
     assert better > 0
+
+
+def _weighted_golden_block():
+    g = load_golden("rfp2_weighted_objective.txt")
+    x = np.zeros(32, np.float32)
+    imp = np.zeros(32, np.float32)
+    cols = [int(c) for c in g["nonzero_columns"]]
+    x[cols] = g["nonzero_values"]
+    imp[cols] = g["importance"]
+    return g, x, imp
+
+
+def test_weighted_objective_golden_block():
+    """The hand-derived block of the golden fixture: sigma^2, the objective's
+    closed-form values at the two contending bytes of each half, and the
+    packed block (0x3F for half 0, 0x40 for half 1) all follow the page's
+    weight importance * sqrt(sigma^2 + x^2); dropping the square root,
+    squaring the importance or dropping sigma^2 would pick other bytes."""
+    g, x, imp = _weighted_golden_block()
+    s2 = oracle.rfp2_block_sigma2(x)
+    assert s2 == g["sigma2"]
+    ra, rb = math.sqrt(s2 + 1.0), math.sqrt(s2 + 14.0625)
+    for h, ia in ((0, 16.0), (1, 48.0)):
+        xs, ws = x[16 * h:16 * h + 16], imp[16 * h:16 * h + 16]
+        assert math.isclose(oracle.rfp2_half_wsse(xs, ws, s2, 0x3F), ia * ra / 256, rel_tol=1e-14)
+        assert math.isclose(oracle.rfp2_half_wsse(xs, ws, s2, 0x40), rb / 16, rel_tol=1e-14)
+    P = oracle.rfp2_pack_weighted(x.reshape(1, 32), imp)
+    assert [int(v) for v in P.ravel()] == [int(v) for v in g["block"]]
+    assert [int(v) for v in P.ravel()[8:]] == [int(v) for v in g["bytes_page_formula"]]
+
+
+def test_weighted_objective_golden_block_separates_mistaken_weights():
+    """The fixture discriminates: an independent brute force over the 127
+    scale bytes (UE4M3 from torch's E4M3FN decoder, halved) reproduces the
+    fixture's bytes for the page's weight and for each mistaken form, and
+    every mistaken form's bytes differ from the page formula's."""
+    g, x, imp = _weighted_golden_block()
+    table = e4m3fn_half_table()
+    s2 = float(g["sigma2"])
+    forms = {
+        "bytes_page_formula": lambda i, v: i * math.sqrt(s2 + v * v),
+        "bytes_without_sqrt": lambda i, v: i * (s2 + v * v),
+        "bytes_importance_squared": lambda i, v: i * i * math.sqrt(s2 + v * v),
+        "bytes_without_sigma2": lambda i, v: i * abs(v),
+    }
+    for key, wfun in forms.items():
+        got = []
+        for h in range(2):
+            xs, ws = x[16 * h:16 * h + 16].astype(np.float64), imp[16 * h:16 * h + 16]
+            best = None
+            for b in range(0x7F):
+                s = float(table[b])
+                err = 0.0
+                for v, i in zip(xs, ws):
+                    inner = s == 0.0 or abs(np.float32(v) / np.float32(s)) <= 2.5
+                    r = 0.0 if s == 0.0 else (1.0 if inner else 4.0) * s * (-1.0 if v < 0 else 1.0)
+                    err += wfun(float(i), float(v)) * (v - r) ** 2
+                if best is None or err < best[0]:
+                    best = (err, b)
+            got.append(best[1])
+        assert got == [int(v) for v in g[key]], key
+        if key != "bytes_page_formula":
+            assert got != [int(v) for v in g["bytes_page_formula"]], key
