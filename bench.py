@@ -226,6 +226,10 @@ def run_gpu(args):
     Wd = torch.from_numpy(w["W"]).cuda()
     P = gl.rfp2_pack_weights(Wd)
     del Wd
+    torch.cuda.synchronize()
+    # the weights are written once, before any timed call: each call may
+    # stream its weights while the previous call is still running
+    gl.rfp2_set_weight_prefetch(True)
     copies = max(4, -(-4 * L2_BYTES // WEIGHT_BYTES))
     copies = 1 << (copies - 1).bit_length()
     Pc = torch.empty((copies,) + tuple(P.shape), dtype=torch.uint8, device="cuda")
@@ -342,8 +346,8 @@ def run_gpu(args):
         },
         "secondary": dict({
             "decode_batch4": {
-                "workload": "same weights, batch 4 through rfp2_gemv (tensor-core path from "
-                            "3 tokens: prep + decode-into-TMEM GEMM)",
+                "workload": "same weights, batch 4 through rfp2_gemv (int8 dp4a path, quantize "
+                            "fused, one launch)",
                 "value": round(WEIGHT_BYTES / (ms_b4 * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "us_per_call": round(ms_b4 * 1e3, 3),
                 "frac_of_hbm_peak": round(WEIGHT_BYTES / (ms_b4 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
@@ -508,6 +512,7 @@ def _sec_decode(torch, gl, peaks, N=1, reps=3):
     w = decode_gemv(N=max(N, 1))
     P = gl.rfp2_pack_weights(torch.from_numpy(w["W"]).cuda())
     torch.cuda.synchronize()
+    gl.rfp2_set_weight_prefetch(True)  # weights written once, before the timed calls
     copies = max(4, -(-4 * L2_BYTES // WEIGHT_BYTES))
     copies = 1 << (copies - 1).bit_length()
     Pc = torch.empty((copies,) + tuple(P.shape), dtype=torch.uint8, device="cuda")

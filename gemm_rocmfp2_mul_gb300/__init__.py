@@ -26,6 +26,7 @@ __all__ = [
     "rfp2_gemv_batched", "rfp2_gemv_batched_workspace_bytes",
     "rfp2_pack_weights", "rfp2_pack_weights_weighted", "hfp4_pack_weights", "rfp2_validate_weights",
     "rfp2_debug_half_partials", "rfp2_debug_wait_timeout", "rfp2_row_bytes", "hfp4_row_bytes",
+    "rfp2_set_weight_prefetch", "rfp2_weight_prefetch",
 ]
 
 MAX_BATCH = 8
@@ -76,6 +77,8 @@ _SIGNATURES = {
     "rfp2_validate_weights": (_I32, [_P, _I64, _P, _P, _P]),
     "rfp2_debug_half_partials": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P]),
     "rfp2_debug_wait_timeout": (_I32, [_P, _P]),
+    "rfp2_set_weight_prefetch": (_I32, [_I32]),
+    "rfp2_weight_prefetch": (_I32, []),
 }
 
 
@@ -200,6 +203,18 @@ def rfp2_gemv(W, M, K, x, y=None, workspace=None, dev_status=None):
     _check(lib().rfp2_gemv(_ptr(W), M, K, _ptr(x), N, _ptr(y), _ptr(ws), ws.numel(),
                            _ptr(dev_status), _stream()), "rfp2_gemv")
     return y
+
+
+def rfp2_set_weight_prefetch(enable: bool) -> None:
+    """Process-wide switch (default off): let the GEMV kernels start reading
+    W before the kernel enqueued just before them has completed.  Turn it on
+    only when no kernel that may still be running on the stream writes W."""
+    _check(lib().rfp2_set_weight_prefetch(1 if enable else 0), "rfp2_set_weight_prefetch")
+
+
+def rfp2_weight_prefetch() -> bool:
+    """The current weight-prefetch setting."""
+    return bool(lib().rfp2_weight_prefetch())
 
 
 def rfp2_gemv_noalloc(W, M, K, x, y=None, dev_status=None):

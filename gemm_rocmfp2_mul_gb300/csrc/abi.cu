@@ -1,4 +1,6 @@
-// ABI bookkeeping of librfp2: status strings, version, per-device SM counts.
+// ABI bookkeeping of librfp2: status strings, version, per-device SM counts,
+// the process-wide weight-prefetch switch.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -75,7 +77,20 @@ int sm_count(int device) {
 
 cudaError_t launch_status() { return cudaGetLastError(); }
 
+// Off by default: every kernel waits for the work enqueued before it on its
+// stream before reading weights.
+static std::atomic<int> g_weight_prefetch{0};
+
+bool weight_prefetch() { return g_weight_prefetch.load(std::memory_order_relaxed) != 0; }
+
 }  // namespace rfp2
+
+extern "C" rfp2_status rfp2_set_weight_prefetch(int enable) {
+    rfp2::g_weight_prefetch.store(enable ? 1 : 0, std::memory_order_relaxed);
+    return RFP2_OK;
+}
+
+extern "C" int rfp2_weight_prefetch(void) { return rfp2::weight_prefetch() ? 1 : 0; }
 
 extern "C" const char *rfp2_status_str(int status) {
     switch (status) {

@@ -80,6 +80,19 @@ RFP2_DEV bool mbar_wait(uint64_t *bar, uint32_t parity) {
     }
 }
 
+// The same for a wait that may last long (a producer waiting for its
+// consumers, possibly for the whole of the previous kernel): it sleeps between
+// probes so that it does not take issue slots from the warps doing the work.
+RFP2_DEV bool mbar_wait_sleepy(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(256);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
 // ---- clusters ----------------------------------------------------------------
 RFP2_DEV uint32_t cluster_ctarank() {
     uint32_t r;
@@ -136,6 +149,13 @@ RFP2_DEV void bulk_g2s_stream(void *smem_dst, const void *gsrc, uint32_t bytes, 
         : "memory");
 }
 
+// Prefetch `bytes` (a multiple of 16, 16-byte aligned address) of global
+// memory into L2.  L2 is the point of coherence, so a prefetch can never make
+// a later read return stale data.
+RFP2_DEV void bulk_prefetch_l2(const void *gsrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
+}
+
 RFP2_DEV uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -161,6 +181,9 @@ RFP2_DEV void named_bar_sync(uint32_t id, uint32_t nthreads) {
 
 int sm_count(int device);
 int current_device();
+// rfp2_set_weight_prefetch: may a kernel read weights before the work
+// enqueued ahead of it on the stream has completed?
+bool weight_prefetch();
 cudaError_t launch_status();  // cudaGetLastError wrapper
 
 inline bool aligned(const void *p, size_t a) {

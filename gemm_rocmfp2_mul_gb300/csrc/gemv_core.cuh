@@ -42,7 +42,7 @@ struct Log2<1> {
 constexpr int bpt_max(int nc) { return nc <= 2 ? RFP2_GEMV_BPT12 : nc <= 4 ? 2 : 1; }
 
 // Activations of one thread: [column][block][half][word] permuted int8 words
-// and the per-block scale dA.
+// and the per-block scale dA times 2^19 (see block_sum_2m19).
 template <int NC, int BPT>
 struct Act {
     uint32_t a[NC][BPT][2][4];
@@ -74,7 +74,7 @@ RFP2_DEV void load_act(Act<NC, BPT> &A, const int8_t *q, const float *d, int K, 
                 const uint4 x1 = q4[SWZ ? act_swizzle(c0 + 1) : c0 + 1];
                 permute_act_half(x0.x, x0.y, x0.z, x0.w, A.a[n][b][0]);
                 permute_act_half(x1.x, x1.y, x1.z, x1.w, A.a[n][b][1]);
-                A.d[n][b] = d[(int64_t)cols[n] * KB + kb0 + b];
+                A.d[n][b] = d[(int64_t)cols[n] * KB + kb0 + b] * 0x1p19f;
             } else {
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
@@ -136,15 +136,11 @@ RFP2_DEV void row_dot(const uint8_t *p, const Act<NC, BPT> &A, float (&out)[NC])
         expand_half(k.lo, wlo);
         expand_half(k.hi, whi);
         float s0, s1;
-        decode_scale_pair(k.scales, s0, s1);
+        placed_scale_pair(k.scales, s0, s1);
 #pragma unroll
-        for (int n = 0; n < NC; ++n) {
-            const float f0 = biased_to_float(half_dot_biased(wlo, A.a[n][b][0]));
-            const float f1 = biased_to_float(half_dot_biased(whi, A.a[n][b][1]));
-            float t = f0 * s0;
-            t = fmaf(f1, s1, t);
-            out[n] = fmaf(t, A.d[n][b], out[n]);
-        }
+        for (int n = 0; n < NC; ++n)
+            out[n] = fmaf(block_sum_2m19(wlo, whi, s0, s1, A.a[n][b][0], A.a[n][b][1]), A.d[n][b],
+                          out[n]);
     }
 }
 
@@ -283,116 +279,6 @@ RFP2_DEV void load_act_to_smem(Ring &r, int lane, uint8_t *dst_q, const int8_t *
             if (i < n) {
                 if (i < nq) tq[act_swizzle(i)] = v[j];
                 else td[i - nq] = v[j];
-            }
-        }
-    }
-    mbar_arrive(r.act_bar);
-}
-
-RFP2_DEV float rcp_approx(float v) {
-    float r;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
-    return r;
-}
-
-// Consumer warps (warp index w of cw): quantize x fp32 [nc, K] into the
-// staged, swizzled activation layout, then arrive (every lane) on the
-// activation barrier; with `gq`/`gd` set, q and d also go to global memory.
-// Same results as the quantize kernel (Q8_1-style blocks: d = amax / 127 and
-// q = roundf(a / d) with IEEE division), computed with few instructions:
-//  * eight lanes per 32-value block, four values per lane, so a warp covers
-//    four blocks per step and QB steps are in flight together;
-//  * q comes from z = a * rcp.approx(d), whose relative error is below
-//    2^-22.  The IEEE quotient fl(a/d) lies within 2^-24 of a/d, so both
-//    round to the same integer unless a/d is within about 2^-21 |z| of a
-//    half-integer; lanes whose z is within 2^-19 |z| of one (or is not
-//    finite) take the IEEE division and roundf instead.  Away from
-//    half-integers z + 1.5*2^23 rounds z to that integer and holds it in its
-//    low mantissa bits; |z| <= 127 (1 + 2^-22) needs no clamp.
-#ifndef RFP2_GEMV_QB
-#define RFP2_GEMV_QB 2
-#endif
-RFP2_DEV void quantize_to_smem(Ring &r, int w, int cw, int lane, const float *__restrict__ x,
-                               int nc, int K, uint8_t *act_q, float *act_d, int8_t *gq,
-                               float *gd) {
-    const int nblk = nc * (K >> 5);
-    constexpr int QB = RFP2_GEMV_QB;
-    const int sub = lane >> 3, l8 = lane & 7;
-    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
-    // every CTA reads all of x at the same moment: start each CTA at a
-    // different block so the requests spread over the L2 slices
-    const int rot = (int)((blockIdx.x * 8u) % (unsigned)nblk);
-    for (int s0 = w * 4; s0 < nblk; s0 += cw * 4 * QB) {
-        float v[QB][4];
-        int bb[QB];
-        bool ok[QB];
-#pragma unroll
-        for (int j = 0; j < QB; ++j) {
-            const int b = s0 + j * cw * 4 + sub;
-            ok[j] = b < nblk;
-            bb[j] = b + rot < nblk ? b + rot : b + rot - nblk;
-            const float *src = x + (int64_t)bb[j] * 32 + l8 * 4;
-            if (!ok[j]) {
-                v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0.0f;
-            } else if (vec) {
-                const float4 t = __ldg(reinterpret_cast<const float4 *>(src));
-                v[j][0] = t.x;
-                v[j][1] = t.y;
-                v[j][2] = t.z;
-                v[j][3] = t.w;
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) v[j][e] = __ldg(src + e);
-            }
-        }
-        float m[QB];
-#pragma unroll
-        for (int j = 0; j < QB; ++j)
-            m[j] = fmaxf(fmaxf(fabsf(v[j][0]), fabsf(v[j][1])), fmaxf(fabsf(v[j][2]), fabsf(v[j][3])));
-#pragma unroll
-        for (int off = 4; off >= 1; off >>= 1)
-#pragma unroll
-            for (int j = 0; j < QB; ++j) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], off));
-        float dd[QB], rc[QB];
-        uint32_t word[QB];
-        bool need = false;
-#pragma unroll
-        for (int j = 0; j < QB; ++j) {
-            dd[j] = __fdiv_rn(m[j], 127.0f);
-            rc[j] = dd[j] != 0.0f ? rcp_approx(dd[j]) : 0.0f;
-            uint32_t wq = 0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float z = v[j][e] * rc[j];
-                const float zb = z + 12582912.0f;
-                const float dist = fabsf(z - (zb - 12582912.0f));
-                need |= !(fmaf(fabsf(z), 0x1p-19f, dist) < 0.5f - 0x1p-30f);
-                wq |= ((uint32_t)(__float_as_int(zb) - 0x4B400000) & 0xFFu) << (8 * e);
-            }
-            word[j] = wq;
-        }
-        if (__any_sync(0xffffffffu, need) && need) {
-#pragma unroll
-            for (int j = 0; j < QB; ++j) {
-                if (dd[j] == 0.0f) continue;
-                uint32_t wq = 0;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float qf = fminf(fmaxf(roundf(__fdiv_rn(v[j][e], dd[j])), -127.0f), 127.0f);
-                    wq |= ((uint32_t)static_cast<int>(qf) & 0xFFu) << (8 * e);
-                }
-                word[j] = wq;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < QB; ++j) {
-            if (!ok[j]) continue;
-            const uint32_t i = (uint32_t)bb[j] * 32 + l8 * 4;
-            *reinterpret_cast<uint32_t *>(act_q + act_swizzle(i >> 4) * 16 + (i & 15)) = word[j];
-            if (l8 == 0) act_d[bb[j]] = dd[j];
-            if (gq) {
-                *reinterpret_cast<uint32_t *>(gq + i) = word[j];
-                if (l8 == 0) gd[bb[j]] = dd[j];
             }
         }
     }

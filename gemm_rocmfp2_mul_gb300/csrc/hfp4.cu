@@ -156,6 +156,7 @@ struct HfpArgs {
     const int *kc;
     const uint4 *frag;
     const float *x;  // FOLD: the activations themselves
+    int w_early;     // FOLD: stream W before the earlier work has completed
 };
 
 // PAIRED (N <= 4): the two f16 pieces of token n are MMA columns 2n and
@@ -208,7 +209,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             int c = 0;
-            // the weight tiles do not depend on earlier kernels: start them first
+            // Without FOLD the split kernel of this call ran first and only
+            // released this launch after the earlier work had completed, so
+            // the weight tiles can start at once.  With FOLD this is the
+            // call's only kernel: W is read before that point only when the
+            // caller turned weight prefetch on.
+            if (FOLD && !a.w_early) pdl_wait();
             for (; c < nchunks && c < S; ++c) {
                 const int ks0 = c * 2 * kChunkBlocks;
                 const int bbytes = FOLD ? 0 : min(2 * kChunkBlocks, nks - ks0) * a.N * 64;
@@ -481,6 +487,7 @@ extern "C" rfp2_status hfp4_gemv(const uint8_t *W, int64_t M, int64_t K, const f
     a.kc = kc;
     a.frag = frag;
     a.x = x;
+    a.w_early = weight_prefetch() ? 1 : 0;
     if (fold)
         return from_cuda(launch(hfp4_gemv_kernel<true, true>, dim3(grid), dim3(kThreads), smem, s,
                                 true, wmap, a));

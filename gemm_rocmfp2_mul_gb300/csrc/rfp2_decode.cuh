@@ -21,8 +21,14 @@
 //    of 1.5 * 2^23, so the int32 sum S reads back as the float 1.5*2^23 + S
 //    (|S| <= 16*4*127 = 8128) and one FADD turns it into an exact float.
 //  * A UE4M3 byte placed at bits 20..27 of a float reads as (8+M)*2^(E-130)
-//    (or M*2^-129 for E = 0, a subnormal); one multiply by 2^119 gives the
-//    scale exactly.  The library is built without flush-to-zero.
+//    (or M*2^-129 for E = 0, a subnormal), i.e. the scale times 2^-119
+//    exactly.  The biased dp4a sum is turned into S * 2^100 by one FFMA, so
+//    the products with the placed scales are (S * s) * 2^-19 exactly and the
+//    2^19 goes into the activation scale dA (no FMUL per scale).  The library
+//    is built without flush-to-zero.
+//  * The selector PRMTs are written as PTX prmt: the selectors never have bit
+//    3 of a nibble set, and __byte_perm would spend an extra instruction per
+//    PRMT clearing it.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -37,24 +43,22 @@ constexpr int kDotBias = 0x4B400000;              // bits of 1.5 * 2^23
 constexpr float kDotBiasF = 12582912.0f;          // 1.5 * 2^23
 constexpr float kTwoPow119 = 6.64613997892457936451903530140172288e+35f;
 
+// PTX prmt (default mode): byte i of the result is byte (sel nibble i) of
+// {b, a}; a nibble with bit 3 set would replicate a sign bit instead.
+RFP2_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
 // 16 selectors (one half) -> four words of int8 weights in the lane order above.
 RFP2_DEV void expand_half(uint32_t c, uint32_t (&w)[4]) {
-#ifdef RFP2_SHIFT_ON_FMA
-    // right shifts as multiply-high by a power of two (FMA pipe, not ALU)
-    const uint32_t s = c & 0x33333333u;
-    const uint32_t t = __umulhi(c & 0xCCCCCCCCu, 1u << 30);
-    w[0] = __byte_perm(kCodebookWord, 0u, s);
-    w[1] = __byte_perm(kCodebookWord, 0u, __umulhi(s, 1u << 16));
-    w[2] = __byte_perm(kCodebookWord, 0u, t);
-    w[3] = __byte_perm(kCodebookWord, 0u, __umulhi(t, 1u << 16));
-#else
     const uint32_t s = c & 0x33333333u;
     const uint32_t t = (c >> 2) & 0x33333333u;
-    w[0] = __byte_perm(kCodebookWord, 0u, s);
-    w[1] = __byte_perm(kCodebookWord, 0u, s >> 16);
-    w[2] = __byte_perm(kCodebookWord, 0u, t);
-    w[3] = __byte_perm(kCodebookWord, 0u, t >> 16);
-#endif
+    w[0] = prmt(kCodebookWord, 0u, s);
+    w[1] = prmt(kCodebookWord, 0u, s >> 16);
+    w[2] = prmt(kCodebookWord, 0u, t);
+    w[3] = prmt(kCodebookWord, 0u, t >> 16);
 }
 
 // 16 int8 activations in natural order (u0 = a0..a3, ..., u3 = a12..a15) ->
@@ -78,13 +82,36 @@ RFP2_DEV int half_dot_biased(const uint32_t (&w)[4], const uint32_t (&a)[4]) {
 
 RFP2_DEV float biased_to_float(int biased) { return __int_as_float(biased) - kDotBiasF; }
 
+// S * 2^100 from the bits of 1.5*2^23 + S: the product with 2^100 and the
+// subtraction of 1.5*2^123 are exact, so one FFMA rounds nothing.
+RFP2_DEV float biased_to_scaled(int biased) {
+    return fmaf(__int_as_float(biased), 0x1p100f, -0x1.8p123f);
+}
+
+// Scale bytes e0 (bits 0..7) and e1 (bits 8..15) of `pair` -> the scales
+// times 2^-119 (UE4M3 byte placed at bits 20..27 of a float; exact, a
+// subnormal for E = 0).
+RFP2_DEV void placed_scale_pair(uint32_t pair, float &s0, float &s1) {
+    s0 = __int_as_float((pair << 20) & 0x0FF00000u);
+    s1 = __int_as_float((pair << 12) & 0x0FF00000u);
+}
+
 // Scale bytes e0 (bits 0..7) and e1 (bits 8..15) of `pair` -> fp32 scales.
-// A UE4M3 byte b placed at bits 20..27 of a float reads as (8+M)*2^(E-130)
-// for E > 0 and M*2^-129 for E = 0 (a subnormal); one multiply by 2^119 gives
-// the scale exactly (the library is built without flush-to-zero).
 RFP2_DEV void decode_scale_pair(uint32_t pair, float &s0, float &s1) {
-    s0 = __int_as_float((pair << 20) & 0x0FF00000u) * kTwoPow119;
-    s1 = __int_as_float((pair << 12) & 0x0FF00000u) * kTwoPow119;
+    placed_scale_pair(pair, s0, s1);
+    s0 *= kTwoPow119;
+    s1 *= kTwoPow119;
+}
+
+// One block against one column: (d0*S0 + d1*S1) * 2^-19, from the expanded
+// halves, the placed scales and the permuted activation words of the block.
+// Multiplying by dA * 2^19 gives the block's contribution dA*(d0*S0 + d1*S1)
+// with the same single rounding of the inner sum as the plain formula.
+RFP2_DEV float block_sum_2m19(const uint32_t (&wlo)[4], const uint32_t (&whi)[4], float s0,
+                              float s1, const uint32_t (&alo)[4], const uint32_t (&ahi)[4]) {
+    const float f0 = biased_to_scaled(half_dot_biased(wlo, alo));
+    const float f1 = biased_to_scaled(half_dot_biased(whi, ahi));
+    return fmaf(f1, s1, f0 * s0);
 }
 
 // One 10-byte block split into its two code words and scale pair.

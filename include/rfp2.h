@@ -41,6 +41,15 @@
  *    gives unspecified values in the affected outputs, never a fault.
  *  - GPU kernels need K % 256 == 0 (so a row of packed weights is a whole
  *    number of 16-byte units); other K return RFP2_EUNSUPPORTED.
+ *  - Ordering: by default no kernel reads W (or any other input) before the
+ *    work enqueued ahead of it on the stream has completed, so W may be
+ *    written by the kernel just before (e.g. rfp2_pack_weights on the same
+ *    stream).  rfp2_set_weight_prefetch(1) lets the GEMV kernels start
+ *    streaming W while that earlier kernel is still running (programmatic
+ *    dependent launch); x, workspaces and outputs are still touched only
+ *    after it has completed.  Turn it on only when no kernel that may still
+ *    be in flight on the stream writes W (weights loaded once and
+ *    synchronized before the decode loop).
  */
 #ifndef RFP2_H
 #define RFP2_H
@@ -73,6 +82,15 @@ const char *rfp2_status_str(int status);
 
 /* Library ABI version (major * 100 + minor). */
 int rfp2_version(void);
+
+/* Weight prefetch across kernel boundaries (process-wide, default 0 = off;
+ * see "Ordering" above).  With 1, rfp2_gemv, rfp2_gemv_q8 and hfp4_gemv may
+ * begin reading W before the kernel enqueued just before them on the stream
+ * has completed, which hides the weight stream of one call behind the
+ * previous one.  Takes effect for calls enqueued after it returns (a CUDA
+ * graph keeps the setting it was captured with).  Always returns RFP2_OK. */
+rfp2_status rfp2_set_weight_prefetch(int enable);
+int rfp2_weight_prefetch(void);
 
 /* Largest batch (activation columns) the GEMV entry points take. */
 #define RFP2_MAX_BATCH 8
@@ -114,11 +132,9 @@ size_t rfp2_gemv_workspace_bytes(int64_t N, int64_t K);
  * 16-byte aligned the call is rfp2_gemv_batched (tensor cores, faster from
  * three tokens on; within about 1e-6 relative of the int path); otherwise the
  * quantization is a separate kernel chained to the dp4a GEMV with
- * programmatic dependent launch.  Either way the GEMV starts
- * streaming W before the kernel enqueued just before it on the stream has
- * finished (x, the workspace and y are touched only after it has), so W must
- * not be written by that preceding kernel: after writing W, synchronize the
- * stream before the first call.
+ * programmatic dependent launch.  W is read only after the work enqueued
+ * before the call has completed, unless rfp2_set_weight_prefetch(1) is in
+ * effect (then the one-launch path starts streaming W early; see "Ordering").
  *   x fp32 [N, K] device; y fp32 [N, M] device; workspace device, at least
  *   rfp2_gemv_workspace_bytes(N, K) bytes, 256-byte aligned; after the call
  *   it holds q int8 [N, K] followed (at offset rounded up to 256) by d.

@@ -48,10 +48,12 @@ def test_workspace_sizes(lib):
     up = lambda v: (v + 255) // 256 * 256
     # q int8 [N, K] rounded up to 256 bytes, then d fp32 [N, K/32]
     assert g.rfp2_gemv_workspace_bytes(1, 4096) == 4096 + 128 * 4
-    # from three tokens the tensor-core path's layout: the same q and d, then
-    # the two f16 activation pieces of a 32-token tile and the exponents
-    assert g.rfp2_gemv_workspace_bytes(3, 256) == up(768) + up(24 * 4) + up(2 * 32 * 256 * 2) + up(3 * 4)
-    assert g.rfp2_gemv_workspace_bytes(3, 256) == g.rfp2_gemv_batched_workspace_bytes(16, 256, 3)
+    # every batch 1..8 runs the int8 path: only q and d
+    assert g.rfp2_gemv_workspace_bytes(3, 256) == up(768) + 24 * 4
+    assert g.rfp2_gemv_workspace_bytes(8, 4096) == 8 * 4096 + 8 * 128 * 4
+    # the verify-batch entry point keeps its own layout: q, d, the two f16
+    # activation pieces of a 32-token tile and the exponents
+    assert g.rfp2_gemv_batched_workspace_bytes(16, 256, 3) == up(768) + up(24 * 4) + up(2 * 32 * 256 * 2) + up(3 * 4)
     assert g.rfp2_gemv_workspace_bytes(0, 256) == 0
 
 

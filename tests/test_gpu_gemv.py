@@ -335,3 +335,51 @@ def test_validate_weights(g):
     bad = host(g.rfp2_validate_weights(dev(P), dev_status=st))
     assert int(bad[0]) == 3 == oracle.rfp2_count_bad_scales(P)
     assert host(st)[0] == 6   # RFP2_EBADSCALE
+
+
+def test_gemv_right_after_packing_on_the_same_stream(g):
+    """Weight prefetch is off by default: rfp2_gemv enqueued right after
+    rfp2_pack_weights on the same stream, with no synchronization between
+    them, reads the freshly packed weights (the destination starts as 0xFF
+    bytes, whose scale bytes are illegal, so stale bytes would show)."""
+    import torch
+    assert not g.rfp2_weight_prefetch()
+    M, K, N = 2048, 4096, 1
+    r_w, r_x = child_rngs(321, 2)
+    W = normal_weights(r_w, M, K, 0.02)
+    x = r_x.standard_normal((N, K)).astype(np.float32)
+    Wd, xd = dev(W), dev(x)
+    torch.cuda.synchronize()
+    P = torch.full((M, K // 32, 10), 0xFF, dtype=torch.uint8, device="cuda")
+    g.rfp2_pack_weights(Wd, out=P)
+    y = host(g.rfp2_gemv(P, M, K, xd))
+    Po = oracle.rfp2_pack(W)
+    q, d = oracle.quantize_act(x)
+    assert np.all(rel_err_rows(y, oracle.rfp2_gemv(Po, M, K, q, d)) <= TOL)
+
+
+@pytest.mark.parametrize("N", [1, 2, 4])
+def test_gemv_with_weight_prefetch(g, N):
+    """With rfp2_set_weight_prefetch(1) the GEMV streams W before the
+    previous kernel on the stream has completed (the weights here were
+    written and synchronized before); back-to-back calls on two weight
+    matrices still match the oracle."""
+    import torch
+    M, K = 1500, 4096
+    rng = child_rngs(400 + N, 4)
+    Ws = [normal_weights(rng[i], M, K, 0.02) for i in range(2)]
+    xs = [rng[2 + i].standard_normal((N, K)).astype(np.float32) for i in range(2)]
+    Ps = [oracle.rfp2_pack(W) for W in Ws]
+    Pd = [dev(P) for P in Ps]
+    xd = [dev(x) for x in xs]
+    torch.cuda.synchronize()
+    g.rfp2_set_weight_prefetch(True)
+    try:
+        ys = [g.rfp2_gemv(Pd[i % 2], M, K, xd[(i // 2) % 2]) for i in range(4)]
+        torch.cuda.synchronize()
+    finally:
+        g.rfp2_set_weight_prefetch(False)
+    for i, y in enumerate(ys):
+        q, d = oracle.quantize_act(xs[(i // 2) % 2])
+        ref = oracle.rfp2_gemv(Ps[i % 2], M, K, q, d)
+        assert np.all(rel_err_rows(host(y), ref) <= TOL)

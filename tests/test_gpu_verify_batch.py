@@ -112,13 +112,17 @@ def test_verify_batch_errors(g):
 
 
 @pytest.mark.parametrize("N", [3, 8])
-def test_gemv_routes_small_batches_to_tensor_path_long_k(g, N):
-    """rfp2_gemv at 3..8 tokens takes the tensor-core path; K = 16384 gives
-    four accumulator read-backs along K."""
+def test_gemv_and_batched_agree_long_k(g, N):
+    """At 3 and 8 tokens and K = 16384 (four accumulator read-backs along K
+    on the tensor cores) both entry points meet the int path's tolerance:
+    rfp2_gemv (int8 dp4a) and rfp2_gemv_batched (tensor cores)."""
     M, K = 160, 16384
     r_w, r_x = child_rngs(N + 99, 2)
     P = oracle.rfp2_pack(normal_weights(r_w, M, K, 0.02))
     x = r_x.standard_normal((N, K)).astype(np.float32)
     y = host(g.rfp2_gemv(dev(P), M, K, dev(x)))
+    yb = host(g.rfp2_gemv_batched(dev(P), M, K, dev(x)))
     q, d = oracle.quantize_act(x)
-    assert np.all(rel_err_rows(y, oracle.rfp2_gemv(P, M, K, q, d)) <= TOL)
+    ref = oracle.rfp2_gemv(P, M, K, q, d)
+    assert np.all(rel_err_rows(y, ref) <= TOL)
+    assert np.all(rel_err_rows(yb, ref) <= TOL)
