@@ -146,7 +146,7 @@ def aggregate_gbs(bytes_per_step: int, ms_per_step_max: float, world: int) -> fl
 # ---------------------------------------------------------------------------
 # ncu traffic figure (only while the kernel sources are those it was taken on)
 
-GEMV_SOURCES = ["gemv.cu", "gemv_core.cuh", "rfp2_decode.cuh", "common.cuh", "quantize.cu"]
+GEMV_SOURCES = ["gemv.cu", "gemv_core.cuh", "rfp2_decode.cuh", "common.cuh", "quantize.cuh"]
 
 
 def gemv_source_hash() -> str:
@@ -161,7 +161,7 @@ def gemv_source_hash() -> str:
 def measured_traffic():
     """dram read+write bytes per GEMV launch from the committed ncu summary,
     or None if the kernel sources changed since that capture."""
-    path = os.path.join(ROOT, "profiles", "gemv_q8_decode_14336x4096_traffic.txt")
+    path = os.path.join(ROOT, "profiles", "gemv_stream_decode_14336x4096_traffic.txt")
     try:
         kv = {}
         with open(path) as f:
@@ -306,7 +306,12 @@ def run_gpu(args):
     torch.cuda.empty_cache()
 
     # ---- the other rows of the hot path on their own workloads
+    global CPU_ROWS
+    CPU_ROWS = not (args.no_cpu_baseline or rank != 0)
     sec = {} if args.no_secondary else secondary(torch, gl, peaks)
+    cpu_sec = {}
+    if CPU_ROWS:
+        cpu_sec["decode_batch4"] = cpu_decode_batch4()
 
     # one launch per step (the batch-1 GEMV quantizes x itself), so the
     # kernel's average launch duration is the graph-timed per-step time
@@ -335,7 +340,7 @@ def run_gpu(args):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "gemv_q8_kernel<1,4,fused quantize> (weights streamed by bulk async copies)",
+            "kernel": "gemv_stream_kernel<1,4,true> (activations quantized in-kernel, weights streamed by bulk async copies)",
             "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"],
             "unit": "GB/s",
@@ -360,6 +365,9 @@ def run_gpu(args):
         "clocks": clk,
         "dev_status": status,
     }
+    for key, row in cpu_sec.items():
+        if key in out["secondary"]:
+            out["secondary"][key]["cpu_oracle"] = row
     if rank == 0:
         if not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -390,6 +398,22 @@ def _sec_moe(torch, gl, peaks, reps=3):
     ws = torch.empty(gl.rfp2_moe_workspace_bytes(T, top_k, K), dtype=torch.uint8, device="cuda")
     touched = len(set(w["ids"].ravel().tolist()))
     nbytes = touched * M * K // 32 * 10
+    cpu = None
+    if CPU_ROWS:
+        import oracle
+        ids = w["ids"]
+        ex = sorted(set(ids.ravel().tolist()))[:4]
+        Pe = {e: oracle.rfp2_pack(moe_expert_weights(2, E, M, K, e)[:64]) for e in ex}
+        pairs = [(t, j) for t in range(T) for j in range(top_k) if int(ids[t, j]) in Pe]
+
+        def moe_step():
+            q, d = oracle.quantize_act(w["x"])
+            for t, j in pairs:
+                oracle.rfp2_gemv(Pe[int(ids[t, j])], 64, K, q[t:t + 1], d[t:t + 1])
+
+        cpu = cpu_row(moe_step, len(ex) * 64 * K // 32 * 10, "GB/s (touched experts' packed bytes)",
+                      f"quantize 16 tokens + {len(pairs)} (token, slot) GEMVs over 64 rows of "
+                      f"{len(ex)} touched experts per step")
     us = _graph_us(torch, lambda i: gl.rfp2_moe_gemv(Pc[i % copies], E, M, K, ids, x, y=y,
                                                      workspace=ws), 200, reps)
     del Pc, ids, x, y, ws
@@ -399,7 +423,8 @@ def _sec_moe(torch, gl, peaks, reps=3):
                     f"touched), seed 2; {copies} copies of all experts rotate",
         "value": round(nbytes / us / 1e3, 1), "unit": "GB/s (touched experts' packed bytes)",
         "us_per_call": round(us, 2), "bytes_per_call": nbytes,
-        "frac_of_hbm_peak": round(nbytes / us / 1e3 / peaks["hbm_gbs"], 4)}}
+        "frac_of_hbm_peak": round(nbytes / us / 1e3 / peaks["hbm_gbs"], 4),
+        **({"cpu_oracle": cpu} if cpu else {})}}
 
 
 def _sec_hfp4(torch, gl, peaks, reps=3):
@@ -412,6 +437,10 @@ def _sec_hfp4(torch, gl, peaks, reps=3):
     copies = 16
     Pc = torch.empty((copies,) + tuple(P.shape), dtype=torch.uint8, device="cuda")
     Pc[:] = P
+    Ph = None
+    if CPU_ROWS:
+        import oracle
+        Ph = oracle.hfp4_pack(w["W"][:256])
     for N in (1, 8):
         x = torch.from_numpy(w["x"][:N].copy()).cuda()
         y = torch.empty((N, M), dtype=torch.float32, device="cuda")
@@ -423,6 +452,12 @@ def _sec_hfp4(torch, gl, peaks, reps=3):
             "value": round(P.numel() / us / 1e3, 1), "unit": "GB/s (packed bytes)",
             "us_per_call": round(us, 2), "bytes_per_call": int(P.numel()),
             "frac_of_hbm_peak": round(P.numel() / us / 1e3 / peaks["hbm_gbs"], 4)}
+        if Ph is not None:
+            import oracle
+            xh = w["x"][:N].copy()
+            out[f"hfp4_gemv_batch{N}"]["cpu_oracle"] = cpu_row(
+                lambda: oracle.hfp4_gemv(Ph, 256, K, xh), Ph.size, "GB/s (packed bytes)",
+                f"GEMV over 256 of {M} rows at batch {N} per step")
     del P, Pc
     torch.cuda.empty_cache()
     return out
@@ -450,6 +485,17 @@ def _sec_gemm(torch, gl, peaks, hfp4=False, reps=3):
     us = _graph_us(torch, fn, 20, reps)
     tflops = 2.0 * M * K * N / us / 1e6
     fmt = "HFP4G32" if hfp4 else "ROCmFP2"
+    cpu = None
+    if CPU_ROWS:
+        import oracle
+        if hfp4:
+            Po = oracle.hfp4_pack(w["W"][:4])
+            gstep = lambda: oracle.hfp4_gemm(Po, 4, K, w["X"])
+        else:
+            Po = oracle.rfp2_pack(w["W"][:4])
+            gstep = lambda: oracle.rfp2_gemm(Po, 4, K, w["X"])
+        cpu = cpu_row(gstep, 2.0 * 4 * N * K, "TFLOP/s",
+                      f"4 of {M} weight rows x {N} tokens x K = {K} per step", scale=1e12)
     yardstick = None
     if not hfp4:
         # cuBLAS bf16 on bf16 weights of the same shape and spread, already
@@ -473,7 +519,8 @@ def _sec_gemm(torch, gl, peaks, hfp4=False, reps=3):
         "frac_of_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),
         "frac_of_bf16_sustained": round(tflops / peaks["bf16_tflops_sustained"], 4),
         "bound": "tensor", "peak_source": peaks["source"] + " bf16_tflops (cuBLAS bf16)",
-        **({"yardstick": yardstick} if yardstick else {})}}
+        **({"yardstick": yardstick} if yardstick else {}),
+        **({"cpu_oracle": cpu} if cpu else {})}}
 
 
 def _sec_verify(torch, gl, peaks, reps=3):
@@ -642,31 +689,87 @@ def _oracle_sample(rows: int):
     import oracle
     from synth import decode_gemv
     if _DECODE_W is None:
-        _DECODE_W = decode_gemv(N=1)
+        _DECODE_W = decode_gemv(N=8)
     w = _DECODE_W
     idx = np.linspace(0, M_DEC - 1, rows).astype(np.int64)
     P = oracle.rfp2_pack(w["W"][idx])
     return oracle, P, w["x"][:1].copy(), idx
 
 
-def cpu_baseline(seconds: float, rows: int = 512):
-    """The oracle (single-threaded C, fp64 dots) timed on a bounded sample of
-    the same workload: quantize x + GEMV over `rows` sampled weight rows,
-    repeated for about `seconds`; scaled to packed-weight GB/s."""
-    orc, P, x, idx = _oracle_sample(rows)
+def host_threads() -> int:
+    """Cores of this process's CPU affinity set."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def _timed_threads(step, threads: int, seconds: float):
+    """Run step() repeatedly on `threads` host threads for about `seconds`
+    (the oracle's ctypes calls release the GIL); returns (total steps,
+    elapsed seconds)."""
+    from concurrent.futures import ThreadPoolExecutor
     t0 = time.perf_counter()
-    n = 0
-    while True:
+    deadline = t0 + seconds
+
+    def worker(_):
+        n = 0
+        while True:
+            step()
+            n += 1
+            if time.perf_counter() >= deadline:
+                return n
+
+    with ThreadPoolExecutor(threads) as ex:
+        counts = list(ex.map(worker, range(threads)))
+    return sum(counts), time.perf_counter() - t0
+
+
+# whether the secondary rows also time the oracle on a sample of their data
+CPU_ROWS = False
+CPU_ROW_SECONDS = 2.0
+
+
+def cpu_row(step, bytes_or_flops: float, unit: str, sample: str, scale: float = 1e9) -> dict:
+    """The oracle's rate on one secondary workload: step() on every core of
+    the affinity set for CPU_ROW_SECONDS."""
+    T = host_threads()
+    n, dt = _timed_threads(step, T, CPU_ROW_SECONDS)
+    return {"value": round(n * bytes_or_flops / dt / scale, 6), "unit": unit, "cores": T,
+            "kind": "oracle", "sample": f"{sample}; {n} steps in {dt:.1f} s"}
+
+
+def cpu_decode_batch4():
+    orc, P, x, idx = _oracle_sample(512)
+    x4 = _DECODE_W["x"][:4].copy()
+
+    def step():
+        q, d = orc.quantize_act(x4)
+        orc.rfp2_gemv(P, 512, K_DEC, q, d)
+
+    return cpu_row(step, 512 * K_DEC // 32 * 10, "GB/s",
+                   f"quantize 4 tokens + GEMV over 512 of {M_DEC} rows per step")
+
+
+def cpu_baseline(seconds: float, rows: int = 512):
+    """The oracle (plain single-threaded C, fp64 dots) on a bounded sample of
+    the same workload: quantize x + GEMV over `rows` sampled weight rows, on
+    one core and then on every core of the affinity set (one independent copy
+    of the step per thread); scaled to packed-weight GB/s."""
+    orc, P, x, idx = _oracle_sample(rows)
+
+    def step():
         q, d = orc.quantize_act(x)
         orc.rfp2_gemv(P, rows, K_DEC, q, d)
-        n += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
-    bytes_done = n * rows * K_DEC // 32 * 10
-    return {"value": round(bytes_done / dt / 1e9, 6), "unit": "GB/s", "cores": 1,
-            "kind": "oracle",
-            "sample": f"{n} x (quantize x + GEMV over {rows} of {M_DEC} rows), {dt:.1f} s"}
+
+    per = rows * K_DEC // 32 * 10
+    n1, dt1 = _timed_threads(step, 1, seconds / 3)
+    T = host_threads()
+    nT, dtT = _timed_threads(step, T, 2 * seconds / 3)
+    return {"value": round(nT * per / dtT / 1e9, 6), "unit": "GB/s", "cores": T,
+            "kind": "oracle", "single_core_value": round(n1 * per / dt1 / 1e9, 6),
+            "sample": f"quantize x + GEMV over {rows} of {M_DEC} decode rows per step; "
+                      f"{n1} steps on 1 core in {dt1:.1f} s, {nT} steps on {T} cores in {dtT:.1f} s"}
 
 
 def run_reference(args):
@@ -684,18 +787,31 @@ def run_reference(args):
     per_row = (time.perf_counter() - t0) / 64
     budget = args.ref_seconds / max(1, args.steps + args.warmup)
     # the oracle packs its sample (about 2 ms a row): keep that preparation short
-    rows = int(min(2048, max(8, budget / max(per_row, 1e-9))))
+    rows = int(min(2048, max(8, host_threads() * budget / max(per_row, 1e-9))))
     orc, P, x, idx = _oracle_sample(rows)
-    for _ in range(args.warmup):
+    T = host_threads()
+    # every step: quantize x + GEMV over the sampled rows, the rows split over
+    # the host cores (contiguous ranges, one oracle call per core)
+    cuts = [rows * i // T for i in range(T + 1)]
+    parts = [np.ascontiguousarray(P[cuts[i]:cuts[i + 1]]) for i in range(T)]
+    from concurrent.futures import ThreadPoolExecutor
+    pool = ThreadPoolExecutor(T)
+
+    def step():
         q, d = orc.quantize_act(x)
-        orc.rfp2_gemv(P, rows, K_DEC, q, d)
+        list(pool.map(lambda p: orc.rfp2_gemv(p, p.shape[0], K_DEC, q, d) if p.shape[0] else None,
+                      parts))
+
+    for _ in range(args.warmup):
+        step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        q, d = orc.quantize_act(x)
-        orc.rfp2_gemv(P, rows, K_DEC, q, d)
+        step()
     dt = time.perf_counter() - t0
+    pool.shutdown()
     value = args.steps * rows * K_DEC // 32 * 10 / dt / 1e9
-    sample = f"each step = quantize x + GEMV over {rows} of {M_DEC} rows ({dt:.1f} s total)"
+    sample = (f"each step = quantize x + GEMV over {rows} of {M_DEC} rows split over {T} cores "
+              f"({dt:.1f} s total)")
     out = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -703,7 +819,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": M_DEC, "K": K_DEC, "batch": 1,
                    "reference": "CPU oracle (plain C, fp64), bounded row sample"},
-        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": T, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

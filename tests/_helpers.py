@@ -87,3 +87,25 @@ def rel_err_rows(y, ref) -> np.ndarray:
     num = np.linalg.norm(y - ref, axis=-1)
     den = np.linalg.norm(ref, axis=-1)
     return num / np.where(den == 0, 1.0, den)
+
+
+def oracle_threads() -> int:
+    import os
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def rows_parallel(fn, W, *args, threads=None):
+    """fn(W[rows], *args) over contiguous row ranges on host threads (the
+    oracle's ctypes calls release the GIL), concatenated along axis 0."""
+    from concurrent.futures import ThreadPoolExecutor
+    W = np.ascontiguousarray(W)
+    n = W.shape[0]
+    t = min(threads or oracle_threads(), max(1, n))
+    cuts = [n * i // t for i in range(t + 1)]
+    with ThreadPoolExecutor(t) as ex:
+        parts = list(ex.map(lambda i: fn(np.ascontiguousarray(W[cuts[i]:cuts[i + 1]]), *args),
+                            range(t)))
+    return np.concatenate(parts, axis=0)

@@ -66,5 +66,6 @@ def test_reference_arm_prints_one_json_line():
     j = json.loads(lines[0])
     assert j["impl"] == "reference" and j["steps"] == 3 and j["warmup"] == 1
     assert j["unit"] == "GB/s" and j["higher_is_better"] is True and j["value"] > 0
-    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] == 1
+    import bench
+    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] == bench.host_threads()
     assert j["e2e"]["h2d_bytes_per_step"] == 0

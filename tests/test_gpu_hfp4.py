@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 from synth import child_rngs, hfp4_gemv as hfp4_workload, normal_weights
-from _helpers import rel_err_rows
+from _helpers import rel_err_rows, rows_parallel
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-5
@@ -80,24 +80,22 @@ def test_hfp4_device_packer_feeds_gemv(g):
 
 
 @pytest.mark.parametrize("N", [1, 8])
-def test_hfp4_full_config_sampled(g, N):
-    """8192 x 8192 N(0, 0.02^2) weights, seed 4, packed on the GPU; the oracle
-    checks 64 sampled rows (packed bytes bit-exact, outputs normwise over the
-    sample); every output is finite."""
+def test_hfp4_full_config(g, N):
+    """8192 x 8192 N(0, 0.02^2) weights, seed 4, packed on the GPU: every
+    packed byte of all 8192 rows bit-exact with the oracle, every output row
+    within tolerance of the oracle (normwise per token over all rows)."""
     import torch
     w = hfp4_workload(N=8)
     M, K = w["W"].shape
     Pg = g.hfp4_pack_weights(dev(w["W"]))
-    rows = np.sort(np.random.default_rng(N).choice(M, 64, replace=False))
-    rows[0], rows[-1] = 0, M - 1
-    Po = oracle.hfp4_pack(w["W"][rows])
-    np.testing.assert_array_equal(host(Pg)[rows], Po)
+    Po = rows_parallel(oracle.hfp4_pack, w["W"])
+    np.testing.assert_array_equal(host(Pg), Po)
     x = w["x"][:N]
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     y = host(g.hfp4_gemv(Pg, M, K, dev(x), dev_status=st))
     assert int(host(st)[0]) == 0
-    ref = oracle.hfp4_gemv(Po, len(rows), K, x)
-    assert np.all(rel_err_rows(y[:, rows], ref) <= TOL)
+    ref = rows_parallel(lambda P, x: oracle.hfp4_gemv(P, P.shape[0], K, x).T, Po, x).T
+    assert np.all(rel_err_rows(y, ref) <= TOL)
     assert np.all(np.isfinite(y))
 
 
