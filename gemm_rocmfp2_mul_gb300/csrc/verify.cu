@@ -376,11 +376,13 @@ __global__ void __launch_bounds__(VTHREADS, 1)
         }
     } else if (warp == 1) {
         // ---- MMA issuer (the whole warp; one elected lane issues): step u =
-        // stages 4u .. 4u+3; stage t reads A slot t % 8 and B stage t % SB,
-        // k-step kk goes to accumulator kk & 1; round r = stages [64r,
-        // 64r + 64) starts both afresh.  The next step's barrier probe is
-        // issued before this step's MMAs; the abort flag is read every other
-        // step.
+        // stages VQ*u .. VQ*u + VQ - 1; stage t reads A slot t % kASlots and
+        // B stage t % SB; k-step kk goes to accumulator kk % NACC; round r =
+        // stages [VROUND*r, VROUND*(r + 1)) starts the accumulators afresh
+        // (32/64-token tiles: VQ 4, 12/8 A slots, rounds of 64 stages, two
+        // accumulators; 128-token tiles: VQ 2, 6 A slots, rounds of 32
+        // stages, one accumulator).  The next step's barrier probe is issued
+        // before this step's MMAs; the abort flag is read every other step.
         constexpr uint32_t idesc = idesc_f16_f32(VBM, NB);
         const uint64_t bdesc0 = smem_desc_sw128(smem_addr(bring));
         const uint32_t a_tmem0 = tmem + (uint32_t)kACol0;

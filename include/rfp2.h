@@ -125,16 +125,13 @@ rfp2_status rfp2_gemv_q8(const uint8_t *W, int64_t M, int64_t K, const int8_t *q
 size_t rfp2_gemv_workspace_bytes(int64_t N, int64_t K);
 
 /* ---------------------------------------------------------------------------
- * ROCmFP2 GEMV from fp32 activations: quantizes x (q then d, written to
- * `workspace`) and runs the GEMV.  For N <= 2 (when the activations fit in
- * shared memory beside a weight ring) the quantization runs inside the GEMV
- * kernel, one launch per call.  For 3 <= N <= 8 with M % 16 == 0 and x
- * 16-byte aligned the call is rfp2_gemv_batched (tensor cores, faster from
- * three tokens on; within about 1e-6 relative of the int path); otherwise the
- * quantization is a separate kernel chained to the dp4a GEMV with
- * programmatic dependent launch.  W is read only after the work enqueued
- * before the call has completed, unless rfp2_set_weight_prefetch(1) is in
- * effect (then the one-launch path starts streaming W early; see "Ordering").
+ * ROCmFP2 GEMV from fp32 activations ("ROCmFP2 codebook research report",
+ * section "03 Runtime"): quantizes x to Q8_1 blocks and runs the int8 dp4a
+ * GEMV in one kernel launch for every batch 1 <= N <= 8; int32 sums per
+ * 16-weight half, scales applied after the integer sums.  W is read only
+ * after the work enqueued before the call has completed, unless
+ * rfp2_set_weight_prefetch(1) is in effect (then the kernel starts streaming
+ * W early; see "Ordering").
  *   x fp32 [N, K] device; y fp32 [N, M] device; workspace device, at least
  *   rfp2_gemv_workspace_bytes(N, K) bytes, 256-byte aligned; after the call
  *   it holds q int8 [N, K] followed (at offset rounded up to 256) by d.
@@ -153,11 +150,13 @@ rfp2_status rfp2_gemv(const uint8_t *W, int64_t M, int64_t K, const float *x, in
  * rfp2_gemv; the quantized activations go to a fixed scratch array inside the
  * library (73,728 bytes of device memory, held on every GPU that loads the
  * library until the process exits).  Limits: N * K <= 65536; larger sizes
- * return RFP2_EWORKSPACE.  The first call on a device looks up the array's
- * device address (cudaGetSymbolAddress); make that first call before any
- * stream capture.  All calls on a device share the array: calls that overlap
- * on the GPU race on it, so the caller serializes them.  Nothing in the array
- * needs clearing; every call overwrites what it uses.
+ * return RFP2_EWORKSPACE.  Every call looks up the array's device address
+ * on the current device (cudaGetSymbolAddress, a host-side query that
+ * allocates nothing), then runs two launches: the quantizer into the array
+ * and the GEMV on pre-quantized input.  All calls on a device share the
+ * array: calls that overlap on the GPU race on it, so the caller serializes
+ * them.  Nothing in the array needs clearing; every call overwrites what it
+ * uses.
  * Errors: as rfp2_gemv_q8, plus EWORKSPACE (N * K too large).
  */
 rfp2_status rfp2_gemv_noalloc(const uint8_t *W, int64_t M, int64_t K, const float *x, int64_t N,
