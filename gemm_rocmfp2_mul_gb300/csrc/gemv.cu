@@ -5,32 +5,37 @@
 // RESCALE, with each block expanded once for every activation column).
 //
 // GB300 design.  The packed weights (2.5 bits per weight) are the only large
-// stream; the decode is bound by the integer pipe (about 50 cycles of one SM
-// sub-partition per 32 blocks, see rfp2_decode.cuh); the activations of a
-// call have to be read and quantized after the kernel before has completed.
+// stream.  The block decode is bound by the integer pipe (about 23 ALU
+// instructions per block and lane: mask, shifts, PRMTs, scale placement).
+// A call's activations may only be read once the kernel before it has
+// completed, so everything between that release and the first dot product
+// (reading x, quantizing it, publishing it to every warp) lies on the
+// critical path of every call and is kept short.
 //  * Persistent grid, one CTA per SM, two CTAs resident per SM: the next
 //    call's CTA becomes resident as soon as this one starts
 //    (griddepcontrol.launch_dependents at entry), so its weight stream can
 //    overlap this call (when weight prefetch is enabled; see
 //    rfp2_set_weight_prefetch) and its barriers are ready when this call ends.
 //  * CTA i owns the contiguous rows [i*M/G, (i+1)*M/G).  A producer warp
-//    streams them in stages of kRows*RG rows (kRows rows per row group of
-//    consumer warps) with 1-D bulk async copies (L2 evict-first) into a ring of as many
-//    stages as fit; the rows that do not fit are prefetched into L2 at entry.
-//  * The activations are read once per CTA (one bulk copy of x), quantized
-//    by the consumer warps (Q8_1-style, bit-exact) and written to shared
+//    streams them in stages of R*RGS rows with 1-D bulk async copies (L2
+//    evict-first) into a ring of as many stages as fit beside the quantized
+//    activations; the rows beyond the ring are prefetched into L2 at entry.
+//    The consumer warps form H sets that take alternate stages (set h takes
+//    stages h, h + H, ...), so a stage is a small unit of the ring (about
+//    20 KB) while every warp still decodes two rows per stage.
+//  * Each CTA reads x straight from global memory after the release (no
+//    staging copy) and quantizes it (Q8_1-style, bit-exact): four lanes per
+//    32-value block, eight values per lane.  The int8 values go to shared
 //    memory already permuted into the lane order of expand_half, one 16-byte
-//    word group per lane and half-block, so the decode loop reads them with
-//    conflict-free 16-byte loads and keeps no activation registers.
-//  * Each consumer warp takes kRows rows of every stage (independent rows in
-//    flight, one barrier wait per kRows rows), keeps the per-lane partial
-//    sums of up to 16 rows x columns in registers and reduces them across the
-//    warp once per round (a transposing butterfly), so no stage ends with a
-//    shuffle chain and a store.
+//    word per lane and half-block at an offset that is a compile-time
+//    constant from a per-lane base, so the decode loop reads them with
+//    conflict-free 16-byte loads and no address arithmetic.
+//  * After each stage a warp reduces its rows' lane partials across the warp
+//    (a transposing butterfly over R*NC values) and stores them.  Rows split
+//    over several warps along K (very long rows) are combined through a
+//    double-buffered shared-memory slot guarded by mbarriers.
 //  * Every wait is an mbarrier wait with a time limit; a timeout stores
 //    RFP2_ETIMEOUT and the CTA winds down after its copies have landed.
-//    Rows split over several warps along K are combined through a
-//    double-buffered shared-memory slot guarded by mbarriers, never bar.sync.
 #include <mutex>
 
 #include <algorithm>
@@ -42,26 +47,20 @@
 namespace rfp2 {
 namespace {
 
-// Launch shapes (two CTAs per SM; CW consumer warps + 1 producer warp, each
-// consumer decoding R rows of every stage at once).  One column: 16 warps of
-// at most 56 registers, so four warps per SM sub-partition hide each other's
+// Launch shapes: two CTAs per SM; CW consumer warps + 1 producer warp, each
+// consumer decoding kRows rows of a stage at once.  One column: 16 warps of
+// at most 56 registers, four per SM sub-partition to hide each other's
 // latencies.  From two columns the extra activation and accumulator
 // registers would spill at 56, so 8 warps of up to 112 registers.
 #ifndef RFP2_GEMV_WIDE_CW
 #define RFP2_GEMV_WIDE_CW 8
 #endif
-#ifndef RFP2_GEMV_WIDE_R
-#define RFP2_GEMV_WIDE_R 2
-#endif
 template <int NC>
 constexpr int cw_of() {
     return NC == 1 ? 16 : RFP2_GEMV_WIDE_CW;
 }
-template <int NC>
-constexpr int rows_of() {
-    return NC == 1 ? 2 : RFP2_GEMV_WIDE_R;
-}
-// Partial sums (rows x columns) a lane keeps before a warp reduction.
+constexpr int kRows = 2;
+// Values (rows x columns) a warp reduces per stage, padded to a power of two.
 constexpr int kVMax = 16;
 // Shared memory per CTA: two CTAs per SM, or one when a shape needs more.
 constexpr size_t kSmemPair = 113 * 1024;
@@ -70,16 +69,11 @@ constexpr int kMaxStages = 32;
 // Largest batch quantized inside the GEMV kernel by every CTA.
 constexpr int64_t kFusedMaxN = 8;
 
-// Rows of a warp per reduction round: a multiple of R with RR * NC <= 16.
-template <int NC, int R>
-constexpr int round_rows() {
-    return R * (kVMax / (R * NC) > 0 ? kVMax / (R * NC) : 1);
-}
-// Activation groups (four blocks) a warp handles per pass: the K = 4096 case
-// spread evenly over the consumer warps.
+// Activation groups (eight blocks of one column) a warp quantizes per pass:
+// the K = 4096 case spread over the consumer warps, at most four in flight.
 template <int NC, int CW>
 constexpr int act_groups_per_pass() {
-    return 32 * NC / CW < 1 ? 1 : 32 * NC / CW > 4 ? 4 : 32 * NC / CW;
+    return 16 * NC / CW < 1 ? 1 : 16 * NC / CW > 4 ? 4 : 16 * NC / CW;
 }
 
 struct GsArgs {
@@ -91,63 +85,31 @@ struct GsArgs {
     float *dout;
     float *y;
     int32_t *status;
-    int M, K, WK, RG, stages, rows_per_cta, rows_extra, x_tma, w_early;
-    uint32_t off_bars, off_red, off_actq, off_actd, off_x;
+    int M, K, WK, H, stages, rows_per_cta, rows_extra, x_vec, w_early;
+    uint32_t off_bars, off_red, off_actq, off_actd;
 };
 
 // ---------------------------------------------------------------------------
-// Activations in shared memory.  Column n, block B of the row (the K-slice
-// warp wk = B / (32*BPT), lane l = (B / BPT) % 32, b = B % BPT) is slot
-// ((n*WK + wk)*BPT + b) of the dA array [slot][32 lanes] and slots 2*that + h
-// of the word array [slot][32 positions][4 words]: the half's 16 int8 values
-// in the lane order of expand_half (0 2 4 6 | 8 10 12 14 | 1 3 5 7 | 9 11 13
-// 15), lane l of slot s at position l ^ (s & 7).  The XOR keeps the decode's
-// loads of a slot conflict-free (the 32 lanes still fill one 512-byte row)
-// and spreads the stores of eight slots of one lane over all 32 banks.
-// dA is stored times 2^19 (see block_sum_2m19).
+// Activations in shared memory.  Block kb of column n sits with the lane
+// that decodes it: K-slice wk = kb / (32*BPT), lane l = (kb / BPT) % 32,
+// b = kb % BPT.  Its 32 int8 values are two 16-byte words (h = 0, 1: the
+// halves) at word index (((wk*BPT + b)*2 + h)*NC + n)*32 + l, and its scale
+// dA (times 2^19, see block_sum_2m19) is float ((wk*BPT + b)*NC + n)*32 + l.
+// The 16 values of a half are stored as [a0 a2 a4 a6 | a1 a3 a5 a7 | a8 a10
+// a12 a14 | a9 a11 a13 a15] (even and odd positions of each group of eight);
+// the decode reorders the four words into the lane order of expand_half.
+// For fixed (b, h, n) the 32 lanes read 512 consecutive bytes: no bank
+// conflicts, and a lane's offsets from its base are compile-time constants.
 
-RFP2_DEV uint32_t act_word_offset(int slot, int lane) {
-    return ((uint32_t)slot * 32 + (uint32_t)(lane ^ (slot & 7))) * 16;
+RFP2_DEV uint32_t act_word_index(int wk, int b, int h, int n, int l, int BPT, int NC) {
+    return ((((uint32_t)wk * BPT + b) * 2 + h) * NC + n) * 32 + l;
 }
 
-// Store the 4 int8 codes `word` (values 4*l8 .. 4*l8+3 of a block, l8 = lane
-// & 7) of the block handled by this lane's group of eight lanes: lanes 2j and
-// 2j+1 swap their words and each writes one permuted word.  Every lane of the
-// warp must call this (a shuffle).  A group beyond the last one stores
-// nothing; a block beyond K (an idle lane's slot) stores zeros.
-RFP2_DEV void store_permuted(uint8_t *actq, float *actd, uint32_t word, float dA, bool in_range,
-                             bool valid, int slot_b, int lane_c, int lane) {
-    const int l8 = lane & 7;
-    const uint32_t partner = __shfl_xor_sync(0xffffffffu, word, 1);
-    const uint32_t w = (l8 & 1) ? prmt(partner, word, 0x7531u) : prmt(word, partner, 0x6420u);
-    if (!in_range) return;
-    const int h = l8 >> 2, jp = (l8 >> 1) & 1;
-    const int wi = (l8 & 1) ? 2 + jp : jp;
-    const int slot = slot_b * 2 + h;
-    *reinterpret_cast<uint32_t *>(actq + act_word_offset(slot, lane_c) + wi * 4) = valid ? w : 0u;
-    if (l8 == 0) actd[(size_t)slot_b * 32 + lane_c] = valid ? dA * 0x1p19f : 0.0f;
-}
-
-// Work split of the activation pass: groups of four consecutive blocks of a
-// column (the row padded to WK*32*BPT blocks, so idle lanes get zeros), one
-// group per warp instruction, eight lanes per block and four values per lane:
-// the 512 bytes of x a group reads are contiguous.
-struct ActGroup {
-    int n, slot_b, lane_c, B;
-};
-// WK and BPT are powers of two: log_wk = log2(WK), so a column has
-// WK * BPT * 8 = 2^(log_wk + log2(BPT) + 3) groups.
-template <int BPT>
-RFP2_DEV ActGroup act_group(int g, int lane, int log_wk) {
-    constexpr int LB = Log2<BPT>::v;
-    ActGroup r;
-    const int lpc = log_wk + LB + 3;
-    r.n = g >> lpc;
-    r.B = ((g & ((1 << lpc) - 1)) << 2) + (lane >> 3);
-    const int wkq = r.B >> (5 + LB);
-    r.lane_c = (r.B >> LB) & 31;
-    r.slot_b = (((r.n << log_wk) + wkq) << LB) + (r.B & (BPT - 1));
-    return r;
+// Bytes 0 of a, b -> bytes 0, 1 of the result.
+RFP2_DEV uint32_t lo_bytes(uint32_t a, uint32_t b) { return prmt(a, b, 0x0040u); }
+// Four values (low byte of each word) -> one word, first value in byte 0.
+RFP2_DEV uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    return prmt(lo_bytes(a, b), lo_bytes(c, d), 0x5410u);
 }
 
 RFP2_DEV float rcp_approx_f(float v) {
@@ -156,133 +118,158 @@ RFP2_DEV float rcp_approx_f(float v) {
     return r;
 }
 
-// Quantize the NC x K activations (from global x or the bulk-copied shared
-// copy xs) into the permuted shared layout; CTA 0 also writes q and d in
-// natural layout to qout/dout.  Same results as the quantize kernel (d = amax
-// / 127 and q = roundf(a / d), IEEE divisions): q comes from z = a *
-// rcp.approx(d), whose relative error is below 2^-22; the IEEE quotient
-// fl(a/d) lies within 2^-24 of a/d, so both round to the same integer unless
-// a/d is within about 2^-21 |z| of a half-integer; lanes whose z is within
-// 2^-19 |z| of one (or is not finite) take the IEEE division and roundf
-// instead.  Away from half-integers z + 1.5*2^23 rounds z to that integer and
-// holds it in its low mantissa bits; |z| <= 127 (1 + 2^-22) needs no clamp.
-template <int NC, int BPT, int QB, int CW>
-RFP2_DEV void quantize_permuted(const float *__restrict__ xsrc, bool vec, int K, int WK, int w,
-                                int lane, uint8_t *actq, float *actd, int8_t *gq, float *gd) {
+// Work split of the activation pass: a group is eight blocks of one column
+// that eight consecutive lanes l of one K-slice decode (same b), four
+// quantizing lanes per block and eight values per lane.  Group gi of a
+// column-major enumeration: o = gi % 4 (lanes 8o .. 8o+7), then b, then wk,
+// then n.  WK and BPT are powers of two.
+struct ActSlot {
+    int n, wk, b, l, kb;
+};
+template <int BPT>
+RFP2_DEV ActSlot act_slot(int gi, int lane, int log_wk, int WK) {
+    constexpr int LB = Log2<BPT>::v;
+    ActSlot s;
+    const int t = gi >> 2;
+    s.b = t & (BPT - 1);
+    const int t2 = t >> LB;
+    s.wk = t2 & (WK - 1);
+    s.n = t2 >> log_wk;
+    s.l = 8 * (gi & 3) + (lane >> 2);
+    s.kb = (s.wk * 32 + s.l) * BPT + s.b;
+    return s;
+}
+
+// Quantize the NC x K activations (global x) into the permuted shared layout;
+// CTA 0 also writes q and d in natural layout to gq/gd.  Same results as the
+// quantize kernel (d = amax / 127 and q = roundf(a / d), IEEE divisions): q
+// comes from z = a * rcp.approx(d), whose relative error is below 2^-22, so
+// |z - a/d| < 2^-14 (|a/d| <= 127) and the IEEE quotient fl(a/d) lies within
+// 2^-17 of a/d.  Both therefore round to the same integer unless z is within
+// 2^-12 of a half-integer; lanes where it is (or where z is not finite: a
+// subnormal d whose reciprocal overflows) take the IEEE division and roundf.
+// Elsewhere z + 1.5*2^23 rounds z to that integer and holds it, in two's
+// complement, in the low byte of its bits.
+template <int NC, int BPT, int QP, int CW>
+RFP2_DEV void quantize_to_smem(const float *__restrict__ x, bool vec, int K, int WK, int log_wk,
+                               int warp, int lane, uint8_t *actq, float *actd, int8_t *gq,
+                               float *gd) {
     const int KB = K >> 5;
-    const int ngroups = NC * WK * BPT * 8;
-    const int log_wk = __ffs(WK) - 1;
-    const int l8 = lane & 7;
-    for (int g0 = w; g0 < ngroups; g0 += CW * QB) {
-        float v[QB][4];
-        ActGroup G[QB];
-        bool ok[QB], in[QB];
+    const int ngroups = NC * WK * BPT * 4;
+    const int quarter = lane & 3, h = quarter >> 1, part = quarter & 1;
+    for (int g0 = warp; g0 < ngroups; g0 += CW * QP) {
+        float v[QP][8];
+        ActSlot s[QP];
+        bool in[QP], ok[QP];
 #pragma unroll
-        for (int j = 0; j < QB; ++j) {
-            const int g = g0 + j * CW;
-            in[j] = g < ngroups;
-            G[j] = act_group<BPT>(in[j] ? g : 0, lane, log_wk);
-            ok[j] = in[j] && G[j].B < KB;
-            const float *src = xsrc + (int64_t)G[j].n * K + (int64_t)G[j].B * 32 + l8 * 4;
-            if (!ok[j]) {
-                v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0.0f;
+        for (int i = 0; i < QP; ++i) {
+            const int gi = g0 + i * CW;
+            in[i] = gi < ngroups;  // the same for the whole warp
+            s[i] = act_slot<BPT>(in[i] ? gi : 0, lane, log_wk, WK);
+            ok[i] = in[i] && s[i].kb < KB;
+            const float *src = x + (size_t)s[i].n * K + (size_t)s[i].kb * 32 + quarter * 8;
+            if (!ok[i]) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[i][e] = 0.0f;
             } else if (vec) {
-                const float4 t = *reinterpret_cast<const float4 *>(src);
-                v[j][0] = t.x;
-                v[j][1] = t.y;
-                v[j][2] = t.z;
-                v[j][3] = t.w;
+                const float4 t0 = *reinterpret_cast<const float4 *>(src);
+                const float4 t1 = *reinterpret_cast<const float4 *>(src + 4);
+                v[i][0] = t0.x, v[i][1] = t0.y, v[i][2] = t0.z, v[i][3] = t0.w;
+                v[i][4] = t1.x, v[i][5] = t1.y, v[i][6] = t1.z, v[i][7] = t1.w;
             } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) v[j][e] = src[e];
+                for (int e = 0; e < 8; ++e) v[i][e] = src[e];
             }
         }
-        float m[QB];
 #pragma unroll
-        for (int j = 0; j < QB; ++j)
-            m[j] = fmaxf(fmaxf(fabsf(v[j][0]), fabsf(v[j][1])), fmaxf(fabsf(v[j][2]), fabsf(v[j][3])));
+        for (int i = 0; i < QP; ++i) {
+            float m = fabsf(v[i][0]);
 #pragma unroll
-        for (int off = 4; off >= 1; off >>= 1)
+            for (int e = 1; e < 8; ++e) m = fmaxf(m, fabsf(v[i][e]));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            const float d = __fdiv_rn(m, 127.0f);
+            const float rc = d != 0.0f ? rcp_approx_f(d) : 0.0f;
+            uint32_t qb[8];
+            bool need = false;
 #pragma unroll
-            for (int j = 0; j < QB; ++j) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], off));
-        float dd[QB];
-        uint32_t word[QB];
-        bool need = false;
-#pragma unroll
-        for (int j = 0; j < QB; ++j) {
-            dd[j] = __fdiv_rn(m[j], 127.0f);
-            const float rc = dd[j] != 0.0f ? rcp_approx_f(dd[j]) : 0.0f;
-            uint32_t wq = 0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float z = v[j][e] * rc;
+            for (int e = 0; e < 8; ++e) {
+                const float z = v[i][e] * rc;
                 const float zb = z + 12582912.0f;
-                const float dist = fabsf(z - (zb - 12582912.0f));
-                need |= !(fmaf(fabsf(z), 0x1p-19f, dist) < 0.5f - 0x1p-30f);
-                wq |= ((uint32_t)(__float_as_int(zb) - 0x4B400000) & 0xFFu) << (8 * e);
+                const float t = z - (zb - 12582912.0f);
+                need |= !(fabsf(t) <= 0.5f - 0x1p-12f);
+                qb[e] = __float_as_uint(zb);
             }
-            word[j] = wq;
-        }
-        if (__any_sync(0xffffffffu, need) && need) {
+            if (__any_sync(0xffffffffu, need) && need && d != 0.0f) {
 #pragma unroll
-            for (int j = 0; j < QB; ++j) {
-                if (dd[j] == 0.0f) continue;
-                uint32_t wq = 0;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float qf = fminf(fmaxf(roundf(__fdiv_rn(v[j][e], dd[j])), -127.0f), 127.0f);
-                    wq |= ((uint32_t)static_cast<int>(qf) & 0xFFu) << (8 * e);
+                for (int e = 0; e < 8; ++e) {
+                    const float qf = fminf(fmaxf(roundf(__fdiv_rn(v[i][e], d)), -127.0f), 127.0f);
+                    qb[e] = (uint32_t) static_cast<int>(qf);
                 }
-                word[j] = wq;
             }
-        }
-#pragma unroll
-        for (int j = 0; j < QB; ++j) {
-            store_permuted(actq, actd, word[j], dd[j], in[j], ok[j], G[j].slot_b, G[j].lane_c, lane);
-            if (gq && ok[j]) {
-                *reinterpret_cast<uint32_t *>(gq + (int64_t)G[j].n * K + (int64_t)G[j].B * 32 + l8 * 4) =
-                    word[j];
-                if (l8 == 0) gd[(int64_t)G[j].n * KB + G[j].B] = dd[j];
+            if (!in[i]) continue;
+            const uint32_t ev = pack4(qb[0], qb[2], qb[4], qb[6]);
+            const uint32_t od = pack4(qb[1], qb[3], qb[5], qb[7]);
+            const uint32_t wi = act_word_index(s[i].wk, s[i].b, h, s[i].n, s[i].l, BPT, NC);
+            *reinterpret_cast<uint2 *>(actq + wi * 16 + part * 8) =
+                ok[i] ? make_uint2(ev, od) : make_uint2(0u, 0u);
+            if (quarter == 0)
+                actd[(((size_t)s[i].wk * BPT + s[i].b) * NC + s[i].n) * 32 + s[i].l] =
+                    ok[i] ? d * 0x1p19f : 0.0f;
+            if (gq && ok[i]) {
+                const size_t e0 = (size_t)s[i].n * K + (size_t)s[i].kb * 32 + quarter * 8;
+                *reinterpret_cast<uint2 *>(gq + e0) = make_uint2(
+                    pack4(qb[0], qb[1], qb[2], qb[3]), pack4(qb[4], qb[5], qb[6], qb[7]));
+                if (quarter == 0) gd[(size_t)s[i].n * KB + s[i].kb] = d;
             }
         }
     }
 }
 
-// Pre-quantized q/d from global memory into the permuted shared layout.
-template <int NC, int BPT, int QB, int CW>
-RFP2_DEV void permute_quantized(const int8_t *__restrict__ q, const float *__restrict__ d, int K,
-                                int WK, int w, int lane, uint8_t *actq, float *actd) {
+// Pre-quantized q/d (natural layout, global memory) into the permuted shared
+// layout, with the same work split.
+template <int NC, int BPT, int QP, int CW>
+RFP2_DEV void permute_to_smem(const int8_t *__restrict__ q, const float *__restrict__ d, int K,
+                              int WK, int log_wk, int warp, int lane, uint8_t *actq,
+                              float *actd) {
     const int KB = K >> 5;
-    const int ngroups = NC * WK * BPT * 8;
-    const int log_wk = __ffs(WK) - 1;
-    const int l8 = lane & 7;
-    for (int g0 = w; g0 < ngroups; g0 += CW * QB) {
-        uint32_t word[QB];
-        float dv[QB];
-        ActGroup G[QB];
-        bool ok[QB], in[QB];
+    const int ngroups = NC * WK * BPT * 4;
+    const int quarter = lane & 3, h = quarter >> 1, part = quarter & 1;
+    for (int g0 = warp; g0 < ngroups; g0 += CW * QP) {
+        uint2 w[QP];
+        float dv[QP];
+        ActSlot s[QP];
+        bool in[QP], ok[QP];
 #pragma unroll
-        for (int j = 0; j < QB; ++j) {
-            const int g = g0 + j * CW;
-            in[j] = g < ngroups;
-            G[j] = act_group<BPT>(in[j] ? g : 0, lane, log_wk);
-            ok[j] = in[j] && G[j].B < KB;
-            word[j] = ok[j] ? __ldg(reinterpret_cast<const uint32_t *>(
-                                  q + (int64_t)G[j].n * K + (int64_t)G[j].B * 32 + l8 * 4))
-                            : 0u;
-            dv[j] = ok[j] ? __ldg(d + (int64_t)G[j].n * KB + G[j].B) : 0.0f;
+        for (int i = 0; i < QP; ++i) {
+            const int gi = g0 + i * CW;
+            in[i] = gi < ngroups;
+            s[i] = act_slot<BPT>(in[i] ? gi : 0, lane, log_wk, WK);
+            ok[i] = in[i] && s[i].kb < KB;
+            w[i] = ok[i] ? __ldg(reinterpret_cast<const uint2 *>(
+                               q + (size_t)s[i].n * K + (size_t)s[i].kb * 32 + quarter * 8))
+                         : make_uint2(0u, 0u);
+            dv[i] = ok[i] ? __ldg(d + (size_t)s[i].n * KB + s[i].kb) : 0.0f;
         }
 #pragma unroll
-        for (int j = 0; j < QB; ++j)
-            store_permuted(actq, actd, word[j], dv[j], in[j], ok[j], G[j].slot_b, G[j].lane_c, lane);
+        for (int i = 0; i < QP; ++i) {
+            if (!in[i]) continue;
+            const uint32_t wi = act_word_index(s[i].wk, s[i].b, h, s[i].n, s[i].l, BPT, NC);
+            *reinterpret_cast<uint2 *>(actq + wi * 16 + part * 8) =
+                make_uint2(prmt(w[i].x, w[i].y, 0x6420u), prmt(w[i].x, w[i].y, 0x7531u));
+            if (quarter == 0)
+                actd[(((size_t)s[i].wk * BPT + s[i].b) * NC + s[i].n) * 32 + s[i].l] =
+                    dv[i] * 0x1p19f;
+        }
     }
 }
 
 // ---------------------------------------------------------------------------
-// Decode of R rows (of one stage, row_stride apart) against the activations:
-// acc[r][n] += sum over the lane's BPT blocks of dA*(d0*S0 + d1*S1), each
-// block's sum formed as (d0*S0 + d1*S1) * 2^-19 by block_sum_2m19 and
-// multiplied by the stored dA * 2^19.  The R rows share every activation load.
+// Decode of R rows (row_stride apart) against the activations: acc[r][n] +=
+// sum over the lane's BPT blocks of dA*(d0*S0 + d1*S1), each block's sum
+// formed as (d0*S0 + d1*S1) * 2^-19 by block_sum_2m19 and multiplied by the
+// stored dA * 2^19.  The R rows share every activation load; abase/dbase are
+// the lane's activation bases (its K-slice included).
 
 template <int BPT>
 RFP2_DEV void load_row_words(const uint8_t *p, uint32_t (&v)[BPT >= 2 ? 5 * BPT / 2 : 3]) {
@@ -331,8 +318,8 @@ RFP2_DEV Block block_of(const uint32_t (&v)[BPT >= 2 ? 5 * BPT / 2 : 3], int b) 
 }
 
 template <int NC, int BPT, int R>
-RFP2_DEV void decode_rows(const uint8_t *p0, size_t row_stride, const uint8_t *actq,
-                          const float *actd, int wk, int WK, int lane, float (&acc)[R][NC]) {
+RFP2_DEV void decode_rows(const uint8_t *p0, uint32_t row_stride, const uint8_t *abase,
+                          const float *dbase, float (&acc)[R][NC]) {
     constexpr int NW = BPT >= 2 ? 5 * BPT / 2 : 3;
     uint32_t v[R][NW];
 #pragma unroll
@@ -350,12 +337,12 @@ RFP2_DEV void decode_rows(const uint8_t *p0, size_t row_stride, const uint8_t *a
         }
 #pragma unroll
         for (int n = 0; n < NC; ++n) {
-            const int slot_b = (n * WK + wk) * BPT + b;
-            const uint4 q0 = *reinterpret_cast<const uint4 *>(actq + act_word_offset(2 * slot_b, lane));
-            const uint4 q1 = *reinterpret_cast<const uint4 *>(actq + act_word_offset(2 * slot_b + 1, lane));
-            const float dA = actd[(size_t)slot_b * 32 + lane];
-            const uint32_t lo[4] = {q0.x, q0.y, q0.z, q0.w};
-            const uint32_t hi[4] = {q1.x, q1.y, q1.z, q1.w};
+            const uint4 q0 = *reinterpret_cast<const uint4 *>(abase + ((b * 2 + 0) * NC + n) * 512);
+            const uint4 q1 = *reinterpret_cast<const uint4 *>(abase + ((b * 2 + 1) * NC + n) * 512);
+            const float dA = dbase[(b * NC + n) * 32];
+            // stored [even lo | odd lo | even hi | odd hi] -> expand_half's order
+            const uint32_t lo[4] = {q0.x, q0.z, q0.y, q0.w};
+            const uint32_t hi[4] = {q1.x, q1.z, q1.y, q1.w};
 #pragma unroll
             for (int r = 0; r < R; ++r)
                 acc[r][n] = fmaf(block_sum_2m19(wlo[r], whi[r], s0[r], s1[r], lo, hi), dA, acc[r][n]);
@@ -369,50 +356,50 @@ RFP2_DEV void decode_rows(const uint8_t *p0, size_t row_stride, const uint8_t *a
 template <int NC, int BPT, bool FQ>
 __global__ void __launch_bounds__((cw_of<NC>() + 1) * 32, 2) gemv_stream_kernel(const GsArgs a) {
     constexpr int kCW = cw_of<NC>();
-    constexpr int kRows = rows_of<NC>();
+    constexpr int V = NextPow2<kRows * NC>::v;
+    constexpr int L = Log2<V>::v;
     extern __shared__ __align__(128) uint8_t smem[];
     // let the next call's grid become resident at once (beside this CTA); it
     // touches x, y and the workspace only after this grid has completed
     pdl_launch_dependents();
     const int KB = a.K >> 5;
-    const int rowbytes = KB * 10;
-    const int S = a.stages, RG = a.RG, WK = a.WK;
+    const uint32_t rowbytes = (uint32_t)KB * 10;
+    const int S = a.stages, H = a.H, WK = a.WK;
+    const int G = kCW / H;       // warps per set
+    const int RGS = G / WK;      // row groups per set
+    const int SR = kRows * RGS;  // rows per stage
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.off_bars);
     uint64_t *empty = full + S;
     uint64_t *act_bar = empty + S;
-    uint64_t *xbar = act_bar + 1;
-    uint64_t *redfull = xbar + 1;      // [RG][2]
-    uint64_t *redfree = redfull + 2 * RG;  // [RG][2]
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(redfree + 2 * RG);
-    float *red = reinterpret_cast<float *>(smem + a.off_red);  // [RG][2][WK][kVMax]
+    uint64_t *redfull = act_bar + 1;        // [kCW][2] (row-group id, parity)
+    uint64_t *redfree = redfull + 2 * kCW;  // [kCW][2]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(redfree + 2 * kCW);
+    float *red = reinterpret_cast<float *>(smem + a.off_red);  // [row group][2][WK][kVMax]
     uint8_t *actq = smem + a.off_actq;
     float *actd = reinterpret_cast<float *>(smem + a.off_actd);
-    float *xs = reinterpret_cast<float *>(smem + a.off_x);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bx = blockIdx.x;
     const int64_t r_begin = (int64_t)bx * a.rows_per_cta + min(bx, a.rows_extra);
     const int nrows = a.rows_per_cta + (bx < a.rows_extra ? 1 : 0);
-    // a stage holds kRows rows per row group (rows rg, RG + rg, ... of it)
-    const int nchunks = (nrows + kRows * RG - 1) / (kRows * RG);
-    const uint32_t chunk_bytes = (uint32_t)(kRows * RG) * rowbytes;
+    const int nstages = (nrows + SR - 1) / SR;
+    const uint32_t stage_bytes = (uint32_t)SR * rowbytes;
     const uint8_t *src = a.W + r_begin * rowbytes;
 
+    auto stage_len = [&](int c) { return (uint32_t)min(SR, nrows - c * SR) * rowbytes; };
     auto issue = [&](int c, uint64_t pol) {
         const int s = c % S;
-        const uint32_t bytes = (uint32_t)min(kRows * RG, nrows - c * kRows * RG) * rowbytes;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_g2s_stream(smem + (size_t)s * chunk_bytes, src + (size_t)c * chunk_bytes, bytes,
+        mbar_arrive_expect_tx(&full[s], stage_len(c));
+        bulk_g2s_stream(smem + (size_t)s * stage_bytes, src + (size_t)c * stage_bytes, stage_len(c),
                         &full[s], pol);
     };
 
     if (threadIdx.x == kCW * 32) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kCW);
+            mbar_init(&empty[s], G);
         }
         mbar_init(act_bar, kCW);
-        mbar_init(xbar, 1);
-        for (int i = 0; i < 2 * RG; ++i) {
+        for (int i = 0; i < 2 * kCW; ++i) {
             mbar_init(&redfull[i], WK > 1 ? WK - 1 : 1);
             mbar_init(&redfree[i], 1);
         }
@@ -420,12 +407,10 @@ __global__ void __launch_bounds__((cw_of<NC>() + 1) * 32, 2) gemv_stream_kernel(
         fence_mbar_init();
         // rows beyond the ring: into L2 now (always safe, L2 is coherent), so
         // their copies into the ring later are short
-        for (int c = S; c < nchunks; ++c)
-            bulk_prefetch_l2(src + (size_t)c * chunk_bytes,
-                             (uint32_t)min(kRows * RG, nrows - c * kRows * RG) * rowbytes);
+        for (int c = S; c < nstages; ++c) bulk_prefetch_l2(src + (size_t)c * stage_bytes, stage_len(c));
         if (a.w_early) {
             const uint64_t pol = policy_evict_first();
-            for (int c = 0; c < nchunks && c < S; ++c) issue(c, pol);
+            for (int c = 0; c < nstages && c < S; ++c) issue(c, pol);
         }
     }
     __syncthreads();
@@ -434,19 +419,14 @@ __global__ void __launch_bounds__((cw_of<NC>() + 1) * 32, 2) gemv_stream_kernel(
         // ---- producer
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            pdl_wait();  // the earlier work (x, and W unless prefetching) is complete
-            if (FQ && a.x_tma) {
-                const uint32_t xbytes = (uint32_t)NC * a.K * 4;
-                mbar_arrive_expect_tx(xbar, xbytes);
-                bulk_g2s(xs, a.x, xbytes, xbar);
-            }
+            pdl_wait();  // the earlier work (W unless prefetching) is complete
             int c = 0;
             if (a.w_early) {
-                c = min(nchunks, S);
+                c = min(nstages, S);
             } else {
-                for (; c < nchunks && c < S; ++c) issue(c, pol);
+                for (; c < nstages && c < S; ++c) issue(c, pol);
             }
-            for (; c < nchunks; ++c) {
+            for (; c < nstages; ++c) {
                 const int s = c % S;
                 if (!mbar_wait_sleepy(&empty[s], ((c / S) - 1) & 1)) {
                     record_status(a.status, RFP2_ETIMEOUT);
@@ -463,29 +443,15 @@ __global__ void __launch_bounds__((cw_of<NC>() + 1) * 32, 2) gemv_stream_kernel(
         return;
     }
 
-    // ---- consumers
-    const int wk = warp % WK, rg = warp / WK;
-    const int kb0 = (wk * 32 + lane) * BPT;
-    const bool active = kb0 < KB;
+    // ---- consumers: activations into shared memory, then the stages
+    const int log_wk = __ffs(WK) - 1;
+    constexpr int QP = act_groups_per_pass<NC, kCW>();
     pdl_wait();
     if constexpr (FQ) {
-        constexpr int QB = act_groups_per_pass<NC, kCW>();
-        if (a.x_tma) {
-            if (!mbar_wait(xbar, 0)) {
-                record_status(a.status, RFP2_ETIMEOUT);
-                *abort_flag = 1;
-                return;
-            }
-            quantize_permuted<NC, BPT, QB, kCW>(xs, true, a.K, WK, warp, lane, actq, actd,
-                                           bx == 0 ? a.qout : nullptr, a.dout);
-        } else {
-            const bool vec = (reinterpret_cast<uintptr_t>(a.x) & 15) == 0;
-            quantize_permuted<NC, BPT, QB, kCW>(a.x, vec, a.K, WK, warp, lane, actq, actd,
-                                           bx == 0 ? a.qout : nullptr, a.dout);
-        }
+        quantize_to_smem<NC, BPT, QP, kCW>(a.x, a.x_vec != 0, a.K, WK, log_wk, warp, lane, actq,
+                                           actd, bx == 0 ? a.qout : nullptr, a.dout);
     } else {
-        permute_quantized<NC, BPT, act_groups_per_pass<NC, kCW>(), kCW>(a.q, a.d, a.K, WK, warp, lane,
-                                                                     actq, actd);
+        permute_to_smem<NC, BPT, QP, kCW>(a.q, a.d, a.K, WK, log_wk, warp, lane, actq, actd);
     }
     // one arrival per warp: __syncwarp orders the warp's stores before lane
     // 0's release-arrive, which publishes them to the waiting warps
@@ -497,83 +463,75 @@ __global__ void __launch_bounds__((cw_of<NC>() + 1) * 32, 2) gemv_stream_kernel(
         return;
     }
 
-    constexpr int RR = round_rows<NC, kRows>();
-    constexpr int V = NextPow2<RR * NC>::v;
-    constexpr int L = Log2<V>::v;
-    constexpr int CPR = RR / kRows;  // stages (kRows rows each) per round
-    int round = 0;
-    for (int c0 = 0; c0 < nchunks; c0 += CPR, ++round) {
-        // partial sums of the round, oldest first after the shifts below
-        float part[V];
-#pragma unroll
-        for (int i = 0; i < V; ++i) part[i] = 0.0f;
-        const int npairs = min(CPR, nchunks - c0);
-#pragma unroll 1
-        for (int pi = 0; pi < npairs; ++pi) {
-            const int c = c0 + pi;
-            if (*abort_flag || !mbar_wait(&full[c % S], (c / S) & 1)) {
-                record_status(a.status, RFP2_ETIMEOUT);
-                *abort_flag = 1;
-                return;
-            }
-            // a row past the CTA's last one still lies inside the stage: it is
-            // computed from stale bytes and never stored
-            const uint8_t *p0 = smem + (size_t)(c % S) * chunk_bytes + (size_t)rg * rowbytes +
-                                (active ? (size_t)kb0 * 10 : 0);
-            float acc[kRows][NC];
-#pragma unroll
-            for (int r = 0; r < kRows; ++r)
-#pragma unroll
-                for (int n = 0; n < NC; ++n) acc[r][n] = 0.0f;
-            if (active)
-                decode_rows<NC, BPT, kRows>(p0, (size_t)RG * rowbytes, actq, actd, wk, WK, lane, acc);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[c % S]);
-            // shift in the stage's partials at the top
-#pragma unroll
-            for (int i = 0; i + kRows * NC < V; ++i) part[i] = part[i + kRows * NC];
-#pragma unroll
-            for (int r = 0; r < kRows; ++r)
-#pragma unroll
-                for (int n = 0; n < NC; ++n) part[V - kRows * NC + r * NC + n] = acc[r][n];
+    const int set = warp / G, g = warp - set * G;
+    const int rg = g >> log_wk, wk = g & (WK - 1);
+    const int wid = set * RGS + rg;  // row-group id, < kCW / WK
+    const int kb0 = (wk * 32 + lane) * BPT;
+    const bool active = kb0 < KB;
+    const uint8_t *abase = actq + ((size_t)wk * BPT * 2 * NC * 32 + lane) * 16;
+    const float *dbase = actd + (size_t)wk * BPT * NC * 32 + lane;
+    // a row past the CTA's last one still lies inside the stage: it is
+    // computed from stale bytes and never stored
+    const uint32_t row_off = (uint32_t)(rg * kRows) * rowbytes + (active ? (uint32_t)kb0 * 10 : 0u);
+    // this lane's value after the warp reduction: row vr, column vn
+    const int idx = lane >> (5 - L);
+    const bool writer = (lane & ((32 >> L) - 1)) == 0 && idx < kRows * NC;
+    const int vr = idx / NC, vn = idx - vr * NC;
+    int slot = set % S, phase = (set / S) & 1;
+    int it = 0;  // stages this warp has done
+    for (int c = set; c < nstages; c += H, ++it) {
+        if (*abort_flag || !mbar_wait(&full[slot], phase)) {
+            record_status(a.status, RFP2_ETIMEOUT);
+            *abort_flag = 1;
+            return;
         }
-        // partial index idx holds, counted from the bottom of the live part
-        // (rel = idx - (V - kRows*NC*npairs)), stage c0 + rel / (kRows*NC),
-        // its row (rel / NC) % kRows and column rel % NC
-        float total = warp_transpose_reduce<V>(part, lane);
-        const int idx = lane >> (5 - L);
-        const bool writer = (lane & ((32 >> L) - 1)) == 0;
-        const int rel = idx - (V - kRows * NC * npairs);
-        const int pair = rel >= 0 ? rel / (kRows * NC) : 0;
-        const int rr = rel >= 0 ? (rel / NC) % kRows : 0;
-        const int n = rel >= 0 ? rel % NC : 0;
-        const int64_t row = (int64_t)(c0 + pair) * kRows * RG + rr * RG + rg;
-        const bool store = writer && rel >= 0 && row < nrows;
+        float acc[kRows][NC];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r)
+#pragma unroll
+            for (int n = 0; n < NC; ++n) acc[r][n] = 0.0f;
+        if (active)
+            decode_rows<NC, BPT, kRows>(smem + (size_t)slot * stage_bytes + row_off, rowbytes, abase,
+                                        dbase, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        float vals[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) vals[i] = i < kRows * NC ? acc[i / NC][i % NC] : 0.0f;
+        float total = warp_transpose_reduce<V>(vals, lane);
+        const int row = c * SR + rg * kRows + vr;
+        bool store = writer && row < nrows;
         if (WK > 1) {
-            const int par = round & 1;
-            float *slot = red + ((size_t)(rg * 2 + par) * WK) * kVMax;
+            const int par = it & 1;
+            float *rs = red + (size_t)(wid * 2 + par) * WK * kVMax;
             if (wk != 0) {
-                if (round >= 2 && !mbar_wait(&redfree[rg * 2 + par], ((round >> 1) - 1) & 1)) {
+                if (it >= 2 && !mbar_wait(&redfree[wid * 2 + par], ((it >> 1) - 1) & 1)) {
                     record_status(a.status, RFP2_ETIMEOUT);
                     *abort_flag = 1;
                     return;
                 }
-                if (writer) slot[wk * kVMax + idx] = total;
+                if (writer) rs[wk * kVMax + idx] = total;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&redfull[rg * 2 + par]);
-                continue;
+                if (lane == 0) mbar_arrive(&redfull[wid * 2 + par]);
+                store = false;
+            } else {
+                if (!mbar_wait(&redfull[wid * 2 + par], (it >> 1) & 1)) {
+                    record_status(a.status, RFP2_ETIMEOUT);
+                    *abort_flag = 1;
+                    return;
+                }
+                if (writer)
+                    for (int j = 1; j < WK; ++j) total += rs[j * kVMax + idx];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&redfree[wid * 2 + par]);
             }
-            if (!mbar_wait(&redfull[rg * 2 + par], (round >> 1) & 1)) {
-                record_status(a.status, RFP2_ETIMEOUT);
-                *abort_flag = 1;
-                return;
-            }
-            if (writer)
-                for (int j = 1; j < WK; ++j) total += slot[j * kVMax + idx];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&redfree[rg * 2 + par]);
         }
-        if (store) a.y[(int64_t)n * a.M + r_begin + row] = total;
+        if (store) a.y[(int64_t)vn * a.M + r_begin + row] = total;
+        slot += H;
+        while (slot >= S) {
+            slot -= S;
+            phase ^= 1;
+        }
     }
 }
 
@@ -581,69 +539,71 @@ __global__ void __launch_bounds__((cw_of<NC>() + 1) * 32, 2) gemv_stream_kernel(
 // Host side
 
 struct Plan {
-    int bpt, WK, RG, stages, grid, x_tma;
+    int bpt, WK, H, stages, grid;
     size_t smem;
-    uint32_t off_bars, off_red, off_actq, off_actd, off_x;
+    uint32_t off_bars, off_red, off_actq, off_actd;
 };
 
 size_t align16(size_t v) { return (v + 15) / 16 * 16; }
 
 int cw_for(int NC) { return NC == 1 ? cw_of<1>() : cw_of<2>(); }
-int rows_for(int NC) { return NC == 1 ? rows_of<1>() : rows_of<2>(); }
+
+// K-slices of a row (a power of two) when each lane takes bpt blocks.
+int k_slices(int64_t KB, int bpt) {
+    const int64_t need = (KB + 32 * bpt - 1) / (32 * bpt);
+    int w = 1;
+    while (w < need) w *= 2;
+    return w;
+}
 
 bool make_plan(int NC, int64_t M, int64_t K, bool fq, const void *x, Plan &p) {
-    const int kCW = cw_for(NC), kRows = rows_for(NC);
+    (void)fq;
+    (void)x;
+    const int kCW = cw_for(NC);
     if (K % 256 != 0 || K <= 0 || M <= 0) return false;
     const int64_t KB = K / 32;
     int bpt = 4;
     while (bpt > 1 && KB < 32 * bpt) bpt /= 2;
-    if (KB > (int64_t)kCW * 32 * 4) bpt = 8;
-    const int64_t wk_need = (KB + 32 * bpt - 1) / (32 * bpt);
-    int WK = 0;
-    for (int dv = 1; dv <= kCW; ++dv)
-        if (kCW % dv == 0 && dv >= wk_need) {
-            WK = dv;
-            break;
-        }
-    if (WK == 0) return false;
+    int WK = k_slices(KB, bpt);
+    if (WK > kCW) {
+        bpt = 8;
+        WK = k_slices(KB, bpt);
+    }
+    if (WK > kCW) return false;
+    // two sets of warps on alternate stages where a set still spans a row
+    const int H = (NC == 1 && 2 * WK <= kCW) ? 2 : 1;
+    const int G = kCW / H, RGS = G / WK, SR = kRows * RGS;
     p.bpt = bpt;
     p.WK = WK;
-    p.RG = kCW / WK;
+    p.H = H;
     const int64_t rowbytes = KB * 10;
-    const int64_t chunk = (int64_t)kRows * p.RG * rowbytes;
+    const int64_t stage = (int64_t)SR * rowbytes;
     const int sms = sm_count(current_device());
-    const int64_t chunks_total = (M + kRows * p.RG - 1) / (kRows * p.RG);
-    p.grid = (int)(chunks_total < sms ? chunks_total : sms);
+    const int64_t stages_total = (M + SR - 1) / SR;
+    p.grid = (int)(stages_total < sms ? stages_total : sms);
     const int64_t rows_per_cta = (M + p.grid - 1) / p.grid;
-    const int64_t chunks_per_cta = (rows_per_cta + kRows * p.RG - 1) / (kRows * p.RG);
+    const int64_t stages_per_cta = (rows_per_cta + SR - 1) / SR;
     const size_t actq = (size_t)NC * WK * bpt * 1024;
     const size_t actd = (size_t)NC * WK * bpt * 128;
-    const size_t xbytes = (size_t)NC * K * 4;
-    for (int attempt = 0; attempt < 4; ++attempt) {
-        const size_t budget = attempt < 2 ? kSmemPair : kSmemOne;
-        const bool xt = fq && x && aligned(x, 16) && (attempt % 2 == 0);
-        int S = (int)std::min<int64_t>(chunks_per_cta, kMaxStages);
+    const size_t red = WK > 1 ? (size_t)kCW * 2 * kVMax * 4 : 0;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        const size_t budget = attempt == 0 ? kSmemPair : kSmemOne;
+        int S = (int)std::min<int64_t>(stages_per_cta, kMaxStages);
         for (; S >= 1; --S) {
-            size_t off = (size_t)S * chunk;
-            const size_t bars = align16((size_t)(2 * S + 2 + 4 * p.RG + 1) * 8);
-            const size_t red = WK > 1 ? (size_t)p.RG * 2 * WK * kVMax * 4 : 0;
-            const size_t total = off + bars + red + actq + actd + (xt ? xbytes : 0);
-            if (total <= budget) break;
+            const size_t bars = align16((size_t)(2 * S + 1 + 4 * kCW) * 8 + 4);
+            if ((size_t)S * stage + actq + actd + red + bars <= budget) break;
         }
         if (S < 1) continue;
         p.stages = S;
-        size_t off = (size_t)S * chunk;
-        p.off_bars = (uint32_t)off;
-        off += align16((size_t)(2 * S + 2 + 4 * p.RG + 1) * 8);
-        p.off_red = (uint32_t)off;
-        off += WK > 1 ? (size_t)p.RG * 2 * WK * kVMax * 4 : 0;
+        size_t off = (size_t)S * stage;
         p.off_actq = (uint32_t)off;
         off += actq;
         p.off_actd = (uint32_t)off;
         off += actd;
-        p.off_x = (uint32_t)off;
-        off += xt ? xbytes : 0;
-        p.x_tma = xt ? 1 : 0;
+        p.off_red = (uint32_t)off;
+        off += red;
+        p.off_bars = (uint32_t)off;
+        off += align16((size_t)(2 * S + 1 + 4 * kCW) * 8 + 4);
         p.smem = off;
         return true;
     }
@@ -677,9 +637,9 @@ cudaError_t launch_nc(const Plan &p, GsArgs &a, cudaStream_t stream) {
     }
 }
 
-// One launch: the GEMV on pre-quantized q/d (x == nullptr) or quantizing x
-// itself (q/d copies to qout/dout when given).
-cudaError_t launch_gemv(const uint8_t *W, int64_t M, int64_t K, const int8_t *q, const float *d,
+// One launch for N columns: the GEMV on pre-quantized q/d (x == nullptr) or
+// quantizing x itself (q/d copies to qout/dout when given).
+cudaError_t launch_cols(const uint8_t *W, int64_t M, int64_t K, const int8_t *q, const float *d,
                         const float *x, int64_t N, int8_t *qout, float *dout, float *y,
                         int32_t *status, cudaStream_t stream) {
     const bool fq = x != nullptr;
@@ -697,18 +657,17 @@ cudaError_t launch_gemv(const uint8_t *W, int64_t M, int64_t K, const int8_t *q,
     a.M = (int)M;
     a.K = (int)K;
     a.WK = p.WK;
-    a.RG = p.RG;
+    a.H = p.H;
     a.stages = p.stages;
     a.rows_per_cta = (int)(M / p.grid);
     a.rows_extra = (int)(M % p.grid);
-    a.x_tma = p.x_tma;
+    a.x_vec = fq && aligned(x, 16) ? 1 : 0;
     // without the switch, W is read only after the earlier work completed
     a.w_early = weight_prefetch() ? 1 : 0;
     a.off_bars = p.off_bars;
     a.off_red = p.off_red;
     a.off_actq = p.off_actq;
     a.off_actd = p.off_actd;
-    a.off_x = p.off_x;
     switch (N) {
 #define RFP2_CASE(n)                                                                 \
     case n:                                                                          \
@@ -726,12 +685,35 @@ cudaError_t launch_gemv(const uint8_t *W, int64_t M, int64_t K, const int8_t *q,
     return cudaErrorInvalidValue;
 }
 
+// The GEMV for N columns.  The quantized activations of all columns live in
+// shared memory; when they do not fit beside a weight ring (long rows at
+// several columns), the columns go in groups of as many as fit, one launch
+// each (every group streams W once).
+cudaError_t launch_gemv(const uint8_t *W, int64_t M, int64_t K, const int8_t *q, const float *d,
+                        const float *x, int64_t N, int8_t *qout, float *dout, float *y,
+                        int32_t *status, cudaStream_t stream) {
+    const bool fq = x != nullptr;
+    Plan p;
+    int64_t per = N;
+    while (per > 1 && !make_plan((int)per, M, K, fq, x, p)) --per;
+    const int64_t KB = K / 32;
+    for (int64_t n0 = 0; n0 < N; n0 += per) {
+        const int64_t nc = std::min(per, N - n0);
+        const cudaError_t e = launch_cols(
+            W, M, K, q ? q + n0 * K : nullptr, d ? d + n0 * KB : nullptr, x ? x + n0 * K : nullptr,
+            nc, qout ? qout + n0 * K : nullptr, dout ? dout + n0 * KB : nullptr, y + n0 * M, status,
+            stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 rfp2_status check_gemv_shape(int64_t M, int64_t K, int64_t N, bool fq, const void *x) {
     if (M <= 0 || K <= 0 || N < 1 || N > RFP2_MAX_BATCH) return RFP2_ESHAPE;
     if (M > (1LL << 30) || K > (1LL << 30)) return RFP2_ESHAPE;
     if (K % 256 != 0) return RFP2_EUNSUPPORTED;
-    Plan p;
-    if (!make_plan((int)N, M, K, fq, x, p)) return RFP2_EUNSUPPORTED;
+    Plan p;  // one column always fits when any shape does
+    if (!make_plan(1, M, K, fq, x, p)) return RFP2_EUNSUPPORTED;
     return RFP2_OK;
 }
 

@@ -232,8 +232,18 @@ def test_gemv_q8_parity(g, M, K, N):
 
 
 def test_gemv_max_k(g):
-    # K = 65536 at batch 1: every row spans all twelve consumer warps
+    # K = 65536 at batch 1: every row is split over all sixteen consumer warps
     y, ref = _gemv_case(g, 24, 65536, 1, seed=2)
+    assert np.all(rel_err_rows(y, ref) <= TOL)
+
+
+@pytest.mark.parametrize("M,K,N,fused", [(24, 65536, 8, True), (70, 32768, 7, True),
+                                         (33, 65536, 3, False)])
+def test_gemv_column_groups(g, M, K, N, fused):
+    """Long rows at several columns: the quantized activations of all columns
+    do not fit in shared memory, so the columns run in groups (one launch
+    each); q/d in the workspace and every output row still match."""
+    y, ref = _gemv_case(g, M, K, N, seed=M + N, fused=fused)
     assert np.all(rel_err_rows(y, ref) <= TOL)
 
 
