@@ -401,15 +401,15 @@ def _sec_moe(torch, gl, peaks, reps=3):
     cpu = None
     if CPU_ROWS:
         import oracle
-        ids = w["ids"]
-        ex = sorted(set(ids.ravel().tolist()))[:4]
+        ids_h = w["ids"]
+        ex = sorted(set(ids_h.ravel().tolist()))[:4]
         Pe = {e: oracle.rfp2_pack(moe_expert_weights(2, E, M, K, e)[:64]) for e in ex}
-        pairs = [(t, j) for t in range(T) for j in range(top_k) if int(ids[t, j]) in Pe]
+        pairs = [(t, j) for t in range(T) for j in range(top_k) if int(ids_h[t, j]) in Pe]
 
         def moe_step():
             q, d = oracle.quantize_act(w["x"])
             for t, j in pairs:
-                oracle.rfp2_gemv(Pe[int(ids[t, j])], 64, K, q[t:t + 1], d[t:t + 1])
+                oracle.rfp2_gemv(Pe[int(ids_h[t, j])], 64, K, q[t:t + 1], d[t:t + 1])
 
         cpu = cpu_row(moe_step, len(ex) * 64 * K // 32 * 10, "GB/s (touched experts' packed bytes)",
                       f"quantize 16 tokens + {len(pairs)} (token, slot) GEMVs over 64 rows of "
@@ -534,8 +534,10 @@ def _sec_verify(torch, gl, peaks, reps=3):
     copies = 8
     Pc = torch.empty((copies,) + tuple(P.shape), dtype=torch.uint8, device="cuda")
     Pc[:] = P
+    Po = _oracle_sample(128)[1] if CPU_ROWS else None
     for N in (32, 128):
-        x = torch.from_numpy(np.random.default_rng(N).standard_normal((N, K)).astype(np.float32)).cuda()
+        xh = np.random.default_rng(N).standard_normal((N, K)).astype(np.float32)
+        x = torch.from_numpy(xh).cuda()
         y = torch.empty((N, M), dtype=torch.float32, device="cuda")
         ws = torch.empty(gl.rfp2_gemv_batched_workspace_bytes(M, K, N), dtype=torch.uint8,
                          device="cuda")
@@ -547,6 +549,16 @@ def _sec_verify(torch, gl, peaks, reps=3):
             "value": round(P.numel() / us / 1e3, 1), "unit": "GB/s (packed bytes)",
             "tflops": round(2.0 * M * K * N / us / 1e6, 1),
             "us_per_call": round(us, 2), "bytes_per_call": int(P.numel())}
+        if Po is not None:
+            import oracle
+
+            def vstep(xh=xh):
+                q, d = oracle.quantize_act(xh)
+                oracle.rfp2_gemv(Po, 128, K, q, d)
+
+            out[f"verify_batch{N}"]["cpu_oracle"] = cpu_row(
+                vstep, Po.size, "GB/s (packed bytes)",
+                f"quantize {N} tokens + GEMV over 128 of {M} rows per step")
     del P, Pc
     torch.cuda.empty_cache()
     return out

@@ -385,9 +385,20 @@ __global__ void __launch_bounds__((cw_of<NC>() + 1) * 32, 2) gemv_stream_kernel(
     const uint32_t stage_bytes = (uint32_t)SR * rowbytes;
     const uint8_t *src = a.W + r_begin * rowbytes;
 
+    // Ring slots belong to the sets: set h owns slots h, h + H, ... < S, so
+    // every use of a slot is consumed by the same set, in order (a parity
+    // wait then always refers to the right round).  Stage c = h + H*j goes
+    // to slot h + H*(j % S_h), round j / S_h.
+    auto slot_of = [&](int c, int &round) {
+        const int h = c % H, j = c / H;
+        const int sh = (S - h + H - 1) / H;
+        round = j / sh;
+        return h + H * (j % sh);
+    };
     auto stage_len = [&](int c) { return (uint32_t)min(SR, nrows - c * SR) * rowbytes; };
     auto issue = [&](int c, uint64_t pol) {
-        const int s = c % S;
+        int round;
+        const int s = slot_of(c, round);
         mbar_arrive_expect_tx(&full[s], stage_len(c));
         bulk_g2s_stream(smem + (size_t)s * stage_bytes, src + (size_t)c * stage_bytes, stage_len(c),
                         &full[s], pol);
@@ -427,8 +438,9 @@ __global__ void __launch_bounds__((cw_of<NC>() + 1) * 32, 2) gemv_stream_kernel(
                 for (; c < nstages && c < S; ++c) issue(c, pol);
             }
             for (; c < nstages; ++c) {
-                const int s = c % S;
-                if (!mbar_wait_sleepy(&empty[s], ((c / S) - 1) & 1)) {
+                int round;
+                const int s = slot_of(c, round);
+                if (!mbar_wait_sleepy(&empty[s], (round - 1) & 1)) {
                     record_status(a.status, RFP2_ETIMEOUT);
                     *abort_flag = 1;
                     break;
@@ -436,9 +448,16 @@ __global__ void __launch_bounds__((cw_of<NC>() + 1) * 32, 2) gemv_stream_kernel(
                 if (*abort_flag) break;
                 issue(c, pol);
             }
-            // every copy in flight lands before the CTA may exit
-            for (int i = max(0, c - S); i < c; ++i)
-                if (!mbar_wait(&full[i % S], (i / S) & 1)) record_status(a.status, RFP2_ETIMEOUT);
+            // every copy in flight lands before the CTA may exit: wait for
+            // the latest round issued into each slot (of the first c stages)
+            for (int s = 0; s < S; ++s) {
+                const int h = s % H, jj = s / H, sh = (S - h + H - 1) / H;
+                if (c <= h) continue;
+                const int jmax = (c - 1 - h) / H;  // last issued stage index of set h
+                if (jmax < jj) continue;           // slot never used
+                const int j = jmax - (jmax - jj) % sh;
+                if (!mbar_wait(&full[s], (j / sh) & 1)) record_status(a.status, RFP2_ETIMEOUT);
+            }
         }
         return;
     }
@@ -477,8 +496,8 @@ __global__ void __launch_bounds__((cw_of<NC>() + 1) * 32, 2) gemv_stream_kernel(
     const int idx = lane >> (5 - L);
     const bool writer = (lane & ((32 >> L) - 1)) == 0 && idx < kRows * NC;
     const int vr = idx / NC, vn = idx - vr * NC;
-    int slot = set % S, phase = (set / S) & 1;
-    int it = 0;  // stages this warp has done
+    int slot = set, phase = 0;  // the set's own slots: set, set + H, ... < S
+    int it = 0;                 // stages this warp has done
     for (int c = set; c < nstages; c += H, ++it) {
         if (*abort_flag || !mbar_wait(&full[slot], phase)) {
             record_status(a.status, RFP2_ETIMEOUT);
@@ -528,8 +547,8 @@ __global__ void __launch_bounds__((cw_of<NC>() + 1) * 32, 2) gemv_stream_kernel(
         }
         if (store) a.y[(int64_t)vn * a.M + r_begin + row] = total;
         slot += H;
-        while (slot >= S) {
-            slot -= S;
+        if (slot >= S) {
+            slot = set;
             phase ^= 1;
         }
     }
@@ -570,42 +589,44 @@ bool make_plan(int NC, int64_t M, int64_t K, bool fq, const void *x, Plan &p) {
         WK = k_slices(KB, bpt);
     }
     if (WK > kCW) return false;
-    // two sets of warps on alternate stages where a set still spans a row
-    const int H = (NC == 1 && 2 * WK <= kCW) ? 2 : 1;
-    const int G = kCW / H, RGS = G / WK, SR = kRows * RGS;
     p.bpt = bpt;
     p.WK = WK;
-    p.H = H;
     const int64_t rowbytes = KB * 10;
-    const int64_t stage = (int64_t)SR * rowbytes;
     const int sms = sm_count(current_device());
-    const int64_t stages_total = (M + SR - 1) / SR;
-    p.grid = (int)(stages_total < sms ? stages_total : sms);
-    const int64_t rows_per_cta = (M + p.grid - 1) / p.grid;
-    const int64_t stages_per_cta = (rows_per_cta + SR - 1) / SR;
     const size_t actq = (size_t)NC * WK * bpt * 1024;
     const size_t actd = (size_t)NC * WK * bpt * 128;
     const size_t red = WK > 1 ? (size_t)kCW * 2 * kVMax * 4 : 0;
-    for (int attempt = 0; attempt < 2; ++attempt) {
-        const size_t budget = attempt == 0 ? kSmemPair : kSmemOne;
-        int S = (int)std::min<int64_t>(stages_per_cta, kMaxStages);
-        for (; S >= 1; --S) {
-            const size_t bars = align16((size_t)(2 * S + 1 + 4 * kCW) * 8 + 4);
-            if ((size_t)S * stage + actq + actd + red + bars <= budget) break;
+    // two sets of warps on alternate stages where a set still spans a row
+    // and each set gets at least one ring slot; else one set
+    for (int H = (NC == 1 && 2 * WK <= kCW) ? 2 : 1; H >= 1; --H) {
+        const int G = kCW / H, RGS = G / WK, SR = kRows * RGS;
+        const int64_t stage = (int64_t)SR * rowbytes;
+        const int64_t stages_total = (M + SR - 1) / SR;
+        p.H = H;
+        p.grid = (int)(stages_total < sms ? stages_total : sms);
+        const int64_t rows_per_cta = (M + p.grid - 1) / p.grid;
+        const int64_t stages_per_cta = (rows_per_cta + SR - 1) / SR;
+        for (int attempt = 0; attempt < 2; ++attempt) {
+            const size_t budget = attempt == 0 ? kSmemPair : kSmemOne;
+            int S = (int)std::min<int64_t>(stages_per_cta, kMaxStages);
+            for (; S >= 1; --S) {
+                const size_t bars = align16((size_t)(2 * S + 1 + 4 * kCW) * 8 + 4);
+                if ((size_t)S * stage + actq + actd + red + bars <= budget) break;
+            }
+            if (S < 1 || (S < H && stages_per_cta > 1)) continue;
+            p.stages = S;
+            size_t off = (size_t)S * stage;
+            p.off_actq = (uint32_t)off;
+            off += actq;
+            p.off_actd = (uint32_t)off;
+            off += actd;
+            p.off_red = (uint32_t)off;
+            off += red;
+            p.off_bars = (uint32_t)off;
+            off += align16((size_t)(2 * S + 1 + 4 * kCW) * 8 + 4);
+            p.smem = off;
+            return true;
         }
-        if (S < 1) continue;
-        p.stages = S;
-        size_t off = (size_t)S * stage;
-        p.off_actq = (uint32_t)off;
-        off += actq;
-        p.off_actd = (uint32_t)off;
-        off += actd;
-        p.off_red = (uint32_t)off;
-        off += red;
-        p.off_bars = (uint32_t)off;
-        off += align16((size_t)(2 * S + 1 + 4 * kCW) * 8 + 4);
-        p.smem = off;
-        return true;
     }
     return false;
 }
