@@ -83,6 +83,11 @@ def _load():
                 "orc_hfp4_gemv_rows": (C.c_int, [P, I64, I64, P, I64, P, I64, P]),
                 "orc_f32_to_f16_bits": (C.c_uint16, [C.c_float]),
                 "orc_f16_bits_to_f32": (C.c_float, [C.c_uint16]),
+                "orc_e4m3fn_value": (C.c_double, [C.c_int]),
+                "orc_e4m3fn_encode": (C.c_int, [C.c_double]),
+                "orc_rfp2_to_nvfp4": (C.c_int, [P, I64, I64, P, P]),
+                "orc_nvfp4_quant_act": (C.c_int, [P, I64, I64, P, P, P]),
+                "orc_nvfp4_gemm_rows": (C.c_int, [P, P, I64, I64, P, P, P, I64, P, I64, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(lib, name)
@@ -325,3 +330,49 @@ def f32_to_f16_bits(v: float) -> int:
 
 def f16_bits_to_f32(b: int) -> float:
     return float(_load().orc_f16_bits_to_f32(int(b)))
+
+
+# -- Block-scaled FP4 (NVFP4) form ---------------------------------------------
+
+def e4m3fn_value(b: int) -> float:
+    return float(_load().orc_e4m3fn_value(int(b)))
+
+
+def e4m3fn_encode(v: float) -> int:
+    return int(_load().orc_e4m3fn_encode(float(v)))
+
+
+def rfp2_to_nvfp4(P: np.ndarray, M: int, K: int):
+    """ROCmFP2 blocks -> exact NVFP4 weights: E2M1 codes uint8 [M, K] (one per
+    byte) and E4M3FN scale bytes uint8 [M, K/16]."""
+    P = _c(P, np.uint8)
+    codes = np.zeros((M, K), np.uint8)
+    sb = np.zeros((M, K // 16), np.uint8)
+    _check(_load().orc_rfp2_to_nvfp4(_ptr(P), M, K, _ptr(codes), _ptr(sb)), "rfp2_to_nvfp4")
+    return codes, sb
+
+
+def nvfp4_quant_act(x: np.ndarray):
+    """fp32 x [N, K] -> (E2M1 codes uint8 [N, K], scale bytes uint8 [N, K/16],
+    global factors g fp32 [N]); value = E2M1 * E4M3FN(byte) / g."""
+    x = _c(np.atleast_2d(x), np.float32)
+    N, K = x.shape
+    codes = np.zeros((N, K), np.uint8)
+    sb = np.zeros((N, K // 16), np.uint8)
+    g = np.zeros(N, np.float32)
+    _check(_load().orc_nvfp4_quant_act(_ptr(x), N, K, _ptr(codes), _ptr(sb), _ptr(g)),
+           "nvfp4_quant_act")
+    return codes, sb, g
+
+
+def nvfp4_gemm(wc, ws, M: int, K: int, xc, xs, g, rows=None) -> np.ndarray:
+    """fp64 y [N, len(rows)] = (1/g_n) sum_k wval[m, k] * xval[n, k] with both
+    operands in NVFP4 form."""
+    wc, ws, xc, xs = (_c(a, np.uint8) for a in (wc, ws, xc, xs))
+    g = _c(g, np.float32)
+    N = xc.shape[0]
+    rows = np.arange(M, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    y = np.zeros((N, rows.size), np.float64)
+    _check(_load().orc_nvfp4_gemm_rows(_ptr(wc), _ptr(ws), M, K, _ptr(xc), _ptr(xs), _ptr(g), N,
+                                       _ptr(rows), rows.size, _ptr(y)), "nvfp4_gemm")
+    return y

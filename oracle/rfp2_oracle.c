@@ -19,7 +19,9 @@
  *  [H]  "HFP4" (hipfire.dev quant-formats), sections "Element format (OCP
  *       E2M1)", "Block scale - UE8M0", "Per-row second-level scale (FP16)",
  *       "Byte layout - HFP4G32", "Nibble packing", "Quantization recipe" and
- *       "v1 correctness-anchor inner loop".
+ *       "v1 correctness-anchor inner loop"; its mention of NVIDIA NVFP4
+ *       (16-element blocks with an E4M3 scale) for the block-scaled FP4
+ *       form at the end of this file.
  *
  * Readings where the pages are silent (each is also listed in the design notes):
  *  - Scale search: every legal byte 0x00..0x7E is tried in ascending order and
@@ -570,3 +572,121 @@ uint16_t orc_f32_to_f16_bits(float v)
 }
 
 float orc_f16_bits_to_f32(uint16_t b) { return f16_bits_to_float(b); }
+
+/* ------------------------------------------------------------------------ */
+/* Block-scaled FP4 (NVFP4) form of ROCmFP2.  The pages name NVFP4 only as a
+ * reference format ([H] "HFP4 ... NVIDIA NVFP4": 16-element blocks with an
+ * E4M3 scale).  Readings (no page defines them):
+ *  - An NVFP4 block is 16 E2M1 elements (the lattice above) times one
+ *    E4M3FN scale byte (sign 0; E = bits 3-6, bias 7; E = 0 is subnormal
+ *    M * 2^-9; 0x7F is NaN), times a per-tensor fp32 factor.
+ *  - ROCmFP2 weights need no rounding: [R] 02's closed form makes s(b) half
+ *    the E4M3FN value of the same byte, so codebook * s(b) = (codebook / 2) *
+ *    E4M3FN(b) with codebook / 2 in {-2, -0.5, 0.5, 2}, all E2M1 values.
+ *    The weight factor is 1.
+ *  - Activations (one token row x of K values) follow NVIDIA's published
+ *    recipe, in fp32 as written: g = 2688 / amax(x) (448 * 6; g = 1 for an
+ *    all-zero row); per 16 values t = (bmax / 6) * g, scale byte = E4M3FN of
+ *    t rounded to nearest (ties to even), saturating at 448; element code =
+ *    nearest E2M1 of (x * g) / s (ties to the even mantissa, saturating at
+ *    6; the sign bit follows signbit); a block whose scale byte is 0 stores
+ *    +0 codes.  The value is E2M1 * E4M3FN(byte) / g. */
+
+double orc_e4m3fn_value(int b)
+{
+    int E = (b >> 3) & 15, M = b & 7;
+    double v;
+    if (E == 15 && M == 7) return NAN;
+    v = E == 0 ? M * ldexp(1.0, -9) : (8 + M) * ldexp(1.0, E - 10);
+    return (b & 0x80) ? -v : v;
+}
+
+/* Nearest non-negative E4M3FN byte to v >= 0 (ties to the even byte, which
+ * is the even mantissa), saturating at 0x7E = 448: a search over all bytes. */
+int orc_e4m3fn_encode(double v)
+{
+    int best = 0;
+    double best_err = fabs(v - orc_e4m3fn_value(0));
+    for (int b = 1; b <= 0x7E; b++) {
+        double err = fabs(v - orc_e4m3fn_value(b));
+        if (err < best_err || (err == best_err && (b % 2 == 0) && (best % 2 == 1))) {
+            best = b;
+            best_err = err;
+        }
+    }
+    return best;
+}
+
+/* Weights: codes [M, K] (one E2M1 code per byte) and scale bytes [M, K/16]. */
+int orc_rfp2_to_nvfp4(const uint8_t *P, int64_t M, int64_t K, uint8_t *codes, uint8_t *sbytes)
+{
+    if (!P || !codes || !sbytes || M < 0 || K < 0 || K % 32) return ORC_EINVAL;
+    int64_t KB = K / 32;
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t kb = 0; kb < KB; kb++) {
+            const uint8_t *blk = P + (m * KB + kb) * 10;
+            for (int i = 0; i < 32; i++)
+                codes[m * K + kb * 32 + i] =
+                    (uint8_t)orc_e2m1_encode(orc_codebook_value(blk_code(blk, i)) / 2.0);
+            sbytes[m * (K / 16) + kb * 2] = blk[8];
+            sbytes[m * (K / 16) + kb * 2 + 1] = blk[9];
+        }
+    return ORC_OK;
+}
+
+/* Activations: codes [N, K], scale bytes [N, K/16], g [N] (K % 16 == 0). */
+int orc_nvfp4_quant_act(const float *x, int64_t N, int64_t K, uint8_t *codes, uint8_t *sbytes,
+                        float *g)
+{
+    if (!x || !codes || !sbytes || !g || N < 0 || K < 0 || K % 16) return ORC_EINVAL;
+    for (int64_t n = 0; n < N; n++) {
+        const float *xr = x + n * K;
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; k++)
+            if (fabsf(xr[k]) > amax) amax = fabsf(xr[k]);
+        float gn = amax > 0.0f ? 2688.0f / amax : 1.0f;
+        g[n] = gn;
+        for (int64_t j = 0; j < K / 16; j++) {
+            float bmax = 0.0f;
+            for (int i = 0; i < 16; i++)
+                if (fabsf(xr[j * 16 + i]) > bmax) bmax = fabsf(xr[j * 16 + i]);
+            float t = (bmax / 6.0f) * gn;
+            int b = orc_e4m3fn_encode((double)t);
+            float s = (float)orc_e4m3fn_value(b);
+            sbytes[n * (K / 16) + j] = (uint8_t)b;
+            for (int i = 0; i < 16; i++) {
+                uint8_t c = 0;
+                if (s != 0.0f) {
+                    float u = xr[j * 16 + i] * gn;
+                    float e = u / s;
+                    c = (uint8_t)orc_e2m1_encode((double)e);
+                }
+                codes[n * K + j * 16 + i] = c;
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* y[n, r] = (1 / g[n]) * sum_k E2M1(w[m, k]) E4M3FN(ws[m, k/16]) E2M1(x[n, k])
+ * E4M3FN(xs[n, k/16]) for m = rows[r], in fp64. */
+int orc_nvfp4_gemm_rows(const uint8_t *wc, const uint8_t *ws, int64_t M, int64_t K,
+                        const uint8_t *xc, const uint8_t *xs, const float *g, int64_t N,
+                        const int64_t *rows, int64_t nrows, double *y)
+{
+    if (!wc || !ws || !xc || !xs || !g || !rows || !y || K % 16) return ORC_EINVAL;
+    for (int64_t r = 0; r < nrows; r++) {
+        int64_t m = rows[r];
+        if (m < 0 || m >= M) return ORC_EINVAL;
+        for (int64_t n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; k++) {
+                double w = orc_e2m1_value(wc[m * K + k]) * orc_e4m3fn_value(ws[m * (K / 16) + k / 16]);
+                double a = orc_e2m1_value(xc[n * K + k]) * orc_e4m3fn_value(xs[n * (K / 16) + k / 16]);
+                acc += w * a;
+            }
+            y[n * nrows + r] = acc / (double)g[n];
+        }
+    }
+    return ORC_OK;
+}
