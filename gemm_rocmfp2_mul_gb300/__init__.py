@@ -23,6 +23,7 @@ __all__ = [
     "rfp2_gemv_noalloc",
     "rfp2_moe_gemv", "rfp2_moe_workspace_bytes", "rfp2_gemm", "rfp2_gemm_workspace_bytes",
     "hfp4_gemv", "hfp4_gemv_workspace_bytes", "hfp4_gemm", "hfp4_gemm_workspace_bytes",
+    "rfp2_nvfp4_weight_bytes", "rfp2_to_nvfp4", "rfp2_gemm_nvfp4", "rfp2_gemm_nvfp4_workspace_bytes",
     "rfp2_gemv_batched", "rfp2_gemv_batched_workspace_bytes",
     "rfp2_pack_weights", "rfp2_pack_weights_weighted", "hfp4_pack_weights", "rfp2_validate_weights",
     "rfp2_debug_half_partials", "rfp2_debug_wait_timeout", "rfp2_row_bytes", "hfp4_row_bytes",
@@ -69,6 +70,10 @@ _SIGNATURES = {
     "rfp2_gemv_batched": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
     "hfp4_gemm_workspace_bytes": (_SZ, [_I64, _I64]),
     "hfp4_gemm": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
+    "rfp2_nvfp4_weight_bytes": (_SZ, [_I64, _I64]),
+    "rfp2_to_nvfp4": (_I32, [_P, _I64, _I64, _P, _P]),
+    "rfp2_gemm_nvfp4_workspace_bytes": (_SZ, [_I64, _I64]),
+    "rfp2_gemm_nvfp4": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
     "hfp4_gemv_workspace_bytes": (_SZ, [_I64, _I64]),
     "hfp4_gemv": (_I32, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
     "rfp2_pack_weights": (_I32, [_P, _I64, _I64, _P, _P]),
@@ -307,6 +312,43 @@ def hfp4_gemm(W, M, K, X, Y=None, workspace=None, dev_status=None):
     ws = _workspace(workspace, hfp4_gemm_workspace_bytes(M, K), X)
     _check(lib().hfp4_gemm(_ptr(W), M, K, _ptr(X), N, _ptr(Y), _ptr(ws), ws.numel(),
                            _ptr(dev_status), _stream()), "hfp4_gemm")
+    return Y
+
+
+def rfp2_nvfp4_weight_bytes(M: int, K: int) -> int:
+    return int(lib().rfp2_nvfp4_weight_bytes(M, K))
+
+
+def rfp2_to_nvfp4(W, M, K, out=None):
+    """Exact NVFP4 image of packed ROCmFP2 weights: uint8 [rfp2_nvfp4_weight_bytes]
+    (E2M1 codes [M, K/2], then scale bytes [M, K/16])."""
+    torch = _torch()
+    _need(W, torch.uint8, "W")
+    n = rfp2_nvfp4_weight_bytes(M, K)
+    out = torch.empty(n, dtype=torch.uint8, device=W.device) if out is None else _need(out, torch.uint8, "out")
+    _check(lib().rfp2_to_nvfp4(_ptr(W), M, K, _ptr(out), _stream()), "rfp2_to_nvfp4")
+    return out
+
+
+def rfp2_gemm_nvfp4_workspace_bytes(N: int, K: int) -> int:
+    return int(lib().rfp2_gemm_nvfp4_workspace_bytes(N, K))
+
+
+def rfp2_gemm_nvfp4(Wnv, M, K, X, Y=None, workspace=None, dev_status=None):
+    """NVFP4 prefill GEMM on the FP4 tensor cores: Y fp32 [N, M] = NVFP4(X) Wnv^T
+    (X bf16 [N, K] quantized per token into the workspace)."""
+    torch = _torch()
+    _need(Wnv, torch.uint8, "Wnv")
+    if X.dtype == torch.bfloat16:
+        X = X.view(torch.int16)
+    if X.dtype not in (torch.int16, torch.uint16):
+        raise TypeError("X must be bfloat16 (or its 16-bit pattern)")
+    _need(X, X.dtype, "X")
+    N = X.shape[0]
+    Y = _empty((N, M), torch.float32, X) if Y is None else _need(Y, torch.float32, "Y")
+    ws = _workspace(workspace, rfp2_gemm_nvfp4_workspace_bytes(N, K), X)
+    _check(lib().rfp2_gemm_nvfp4(_ptr(Wnv), M, K, _ptr(X), N, _ptr(Y), _ptr(ws), ws.numel(),
+                                 _ptr(dev_status), _stream()), "rfp2_gemm_nvfp4")
     return Y
 
 

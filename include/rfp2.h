@@ -254,6 +254,43 @@ rfp2_status hfp4_gemm(const uint8_t *W, int64_t M, int64_t K, const uint16_t *X,
                       rfp2_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Block-scaled FP4 (NVFP4) form of the ROCmFP2 prefill GEMM on the FP4 tensor
+ * cores ("ROCmFP2 codebook research report", section "02 Quantization": the
+ * UE4M3 scale s(b) is half the E4M3FN value of the byte, so codebook * s(b) =
+ * (codebook / 2) * E4M3FN(b) with codebook / 2 in {-2, -0.5, 0.5, 2}, all
+ * E2M1 values: a ROCmFP2 block is exactly two NVFP4 blocks).
+ *
+ * rfp2_to_nvfp4: converts packed ROCmFP2 weights W uint8 [M, K/32, 10]
+ *   (2-byte aligned) into the NVFP4 image Wnv (16-byte aligned,
+ *   rfp2_nvfp4_weight_bytes(M, K) bytes): E2M1 codes uint8 [M, K/2] (element
+ *   2j in the low nibble of byte j), then the scale bytes uint8 [M, K/16]
+ *   (the ROCmFP2 scale bytes, unchanged).  Exact.  K % 32 == 0.
+ *   Errors: EINVAL, ESHAPE, EALIGN, ECUDA.
+ *
+ * rfp2_gemm_nvfp4: Y fp32 [N, M] = Xq Wnv^T, where Xq is X (bf16 bit
+ *   patterns [N, K], 16-byte aligned) quantized per token to NVFP4 (NVIDIA's
+ *   published recipe; the pages name NVFP4 only as a reference format): g =
+ *   2688 / amax(row), per 16 values a scale byte E4M3(bmax / 6 * g) rounded
+ *   to nearest even, elements E2M1 of (x * g) / scale rounded to nearest
+ *   even; y = sum(E2M1_w * s_w * E2M1_x * s_x) / g, fp32 accumulation.  The
+ *   activation side is not exact: the result differs from the bf16 GEMM by
+ *   the FP4 rounding of the activations (a few percent of |y|).
+ *   Wnv from rfp2_to_nvfp4; K % 256 == 0; workspace 256-byte aligned of
+ *   rfp2_gemm_nvfp4_workspace_bytes(N, K) bytes; after the call it holds the
+ *   quantized tokens: codes [N, K/2], then (at an offset rounded up to 256)
+ *   scale bytes [N, K/16], then (rounded up to 256) g fp32 [N].
+ *   Errors: EINVAL, ESHAPE, EUNSUPPORTED (K % 256), EWORKSPACE, EALIGN, ECUDA;
+ *   a bounded device wait that ran out stores ETIMEOUT in dev_status.
+ */
+size_t rfp2_nvfp4_weight_bytes(int64_t M, int64_t K);
+rfp2_status rfp2_to_nvfp4(const uint8_t *W, int64_t M, int64_t K, uint8_t *Wnv,
+                          rfp2_stream_t stream);
+size_t rfp2_gemm_nvfp4_workspace_bytes(int64_t N, int64_t K);
+rfp2_status rfp2_gemm_nvfp4(const uint8_t *Wnv, int64_t M, int64_t K, const uint16_t *X,
+                            int64_t N, float *Y, void *workspace, size_t workspace_bytes,
+                            int32_t *dev_status, rfp2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * HFP4G32 GEMV ("HFP4", sections "Per-row second-level scale (FP16)" and
  * "v1 correctness-anchor inner loop"): y[n, m] = row_scale_a(m) *
  * sum_b 2^(e_b - 127) * sum_i E2M1[c_i] * x[n, i], fp32 activations, fp32
