@@ -590,6 +590,59 @@ def _sec_decode(torch, gl, peaks, N=1, reps=3):
         "frac_of_hbm_peak": round(WEIGHT_BYTES / us / 1e3 / peaks["hbm_gbs"], 4)}}
 
 
+def _sec_nvfp4(torch, gl, peaks, reps=3):
+    """Block-scaled FP4 (NVFP4) prefill GEMM 17408 x 5120 x 2048 tokens on the
+    FP4 tensor cores.  The weights convert once (exactly) to the NVFP4 image,
+    like packing; the per-token activation quantization is inside the timed
+    call.  The conversion is timed on its own."""
+    from synth import prefill_gemm
+    w = prefill_gemm()
+    M, K = w["W"].shape
+    N = w["X"].shape[0]
+    Wd = torch.from_numpy(w["W"]).cuda()
+    P = gl.rfp2_pack_weights(Wd)
+    del Wd
+    Wnv = gl.rfp2_to_nvfp4(P, M, K)
+    X = torch.from_numpy(w["X"].view(np.int16)).cuda()
+    Y = torch.empty((N, M), dtype=torch.float32, device="cuda")
+    ws = torch.empty(gl.rfp2_gemm_nvfp4_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
+    us = _graph_us(torch, lambda i: gl.rfp2_gemm_nvfp4(Wnv, M, K, X, Y=Y, workspace=ws), 20, reps)
+    conv_us = _graph_us(torch, lambda i: gl.rfp2_to_nvfp4(P, M, K, out=Wnv), 20, reps)
+    tflops = 2.0 * M * K * N / us / 1e6
+    # nominal dense FP4 : bf16 = 13.5 : 2.25 on this GPU, applied to the measured bf16 peak
+    fp4_peak = peaks["bf16_tflops"] * 6.0
+    Yb = gl.rfp2_gemm(P, M, K, X)
+    torch.cuda.synchronize()
+    dev_bf16 = float((torch.linalg.vector_norm(Y - Yb, dim=1) /
+                      torch.linalg.vector_norm(Yb, dim=1)).max())
+    cpu = None
+    if CPU_ROWS:
+        import oracle
+        Po = oracle.rfp2_pack(w["W"][:4])
+        wc, wsb = oracle.rfp2_to_nvfp4(Po, 4, K)
+        xf = (w["X"].astype(np.uint32) << 16).view(np.float32)
+
+        def nstep():
+            xc, xs, gg = oracle.nvfp4_quant_act(xf)
+            oracle.nvfp4_gemm(wc, wsb, 4, K, xc, xs, gg)
+
+        cpu = cpu_row(nstep, 2.0 * 4 * N * K, "TFLOP/s",
+                      f"quantize {N} tokens + 4 of {M} weight rows x {N} tokens x K = {K} per step",
+                      scale=1e12)
+    del P, Wnv, X, Y, ws, Yb
+    torch.cuda.empty_cache()
+    return {"nvfp4_prefill_gemm": dict({
+        "workload": f"ROCmFP2 [17408, 5120] N(0, 0.015^2) as its exact NVFP4 image x bf16 [2048, 5120] "
+                    f"(0.5% x20) quantized to NVFP4 per call, seed 3",
+        "value": round(tflops, 1), "unit": "TFLOP/s (2*M*N*K, activation quantization included)",
+        "us_per_call": round(us, 1),
+        "frac_of_fp4_peak": round(tflops / fp4_peak, 4),
+        "peak_source": "measured bf16 peak (MEASURED_PEAKS.json) x 6 (nominal dense fp4 : bf16)",
+        "weight_conversion_us": round(conv_us, 1),
+        "max_rel_diff_vs_bf16_gemm": round(dev_bf16, 5),
+        "bound": "tensor"}, **({"cpu_oracle": cpu} if cpu else {}))}
+
+
 SECONDARY_ROWS = {
     "decode1": lambda torch, gl, peaks, reps=3: _sec_decode(torch, gl, peaks, 1, reps),
     "decode4": lambda torch, gl, peaks, reps=3: _sec_decode(torch, gl, peaks, 4, reps),
@@ -598,6 +651,7 @@ SECONDARY_ROWS = {
     "hfp4": _sec_hfp4,
     "gemm": lambda torch, gl, peaks, reps=3: _sec_gemm(torch, gl, peaks, False, reps),
     "hgemm": lambda torch, gl, peaks, reps=3: _sec_gemm(torch, gl, peaks, True, reps),
+    "nvfp4": _sec_nvfp4,
 }
 
 

@@ -20,14 +20,15 @@
 //    codes [N, K/2], scale bytes [N, K/16], g [N].
 //  * The GEMM is persistent over 128-weight-row x 128-token tiles.  A TMA
 //    warp streams 128-byte-wide (256-element) K stages of both code matrices
-//    with the 128-byte swizzle the MMA descriptors expect; four scale warps
-//    write each stage's scale bytes into tensor memory in the layout the
+//    with the 128-byte swizzle the MMA descriptors expect, and the stage's
+//    16 scale bytes of every row and token beside them; four scale warps
+//    copy each stage's scale bytes into tensor memory in the layout the
 //    block-scaled MMA reads (for one MMA of K = 64 the four bytes of row or
 //    token (L % 32) + 32q sit in lane L, every lane quadrant, column base +
 //    q); one thread issues four kind::mxf4nvf4 MMAs per stage into one of two
 //    128-column fp32 accumulators; four epilogue warps read the finished
-//    accumulator, divide by the token's g and store y (consecutive weight
-//    rows in consecutive lanes: coalesced).
+//    accumulator, multiply by the token's 1/g and store y (consecutive
+//    weight rows in consecutive lanes: coalesced).
 //  * Every wait is bounded; a timeout records RFP2_ETIMEOUT and the CTA
 //    winds down after its tensor-core work and copies have completed.
 #include <cuda_fp16.h>
@@ -177,7 +178,9 @@ constexpr int kBKB = 128;  // bytes of K per stage
 constexpr int kSteps = 4;  // MMAs per stage
 constexpr int kNvStages = 6;
 constexpr uint32_t kTileBytes = kBM * kBKB;  // 16 KB, the same for the token tile
-constexpr uint32_t kStageBytes = 2 * kTileBytes;
+constexpr uint32_t kSfTileBytes = kBM * 16;  // 16 scale bytes of each of 128 rows
+// stage: weight codes, token codes, weight scales, token scales
+constexpr uint32_t kStageBytes = 2 * kTileBytes + 2 * kSfTileBytes;
 constexpr uint32_t kNvTmemCols = 512;
 constexpr uint32_t kAccCols = kBN;              // fp32 columns of one accumulator
 constexpr uint32_t kSfCol0 = 2 * kAccCols;      // scale slots after the two accumulators
@@ -216,16 +219,14 @@ RFP2_DEV void tmem_st_16cols(uint32_t taddr, const uint32_t (&r)[16]) {
         : "memory");
 }
 
-// The 16 scale words a lane writes for one stage: column 4h + q holds the
-// four bytes of K-step h of row (or token) base + lane + 32q, which are bytes
-// 4h .. 4h+3 of that row's 16 scale bytes of the stage.
-RFP2_DEV void load_stage_scales(const uint8_t *__restrict__ sf, int64_t rows, int64_t base,
-                                int lane, int64_t row_bytes, int kk, uint32_t (&v)[16]) {
+// The 16 scale words a lane writes for one stage, from the stage's scale
+// tile in shared memory (row r of the tile: its 16 bytes): column 4h + q
+// holds the four bytes of K-step h of row lane + 32q, bytes 4h .. 4h+3 of
+// that row.  The 32 lanes read 512 consecutive bytes per q.
+RFP2_DEV void stage_scales(const uint8_t *tile, int lane, uint32_t (&v)[16]) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const int64_t r = base + lane + 32 * q;
-        const uint4 u = r < rows ? __ldg(reinterpret_cast<const uint4 *>(sf + r * row_bytes + kk * 16))
-                                 : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 u = *reinterpret_cast<const uint4 *>(tile + (lane + 32 * q) * 16);
         v[q] = u.x;
         v[4 + q] = u.y;
         v[8 + q] = u.z;
@@ -235,7 +236,7 @@ RFP2_DEV void load_stage_scales(const uint8_t *__restrict__ sf, int64_t rows, in
 
 __global__ void __launch_bounds__(kNvThreads, 1)
     nv_gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
-                   const uint8_t *__restrict__ wsf, const uint8_t *__restrict__ xsf,
+                   const __grid_constant__ CUtensorMap wsmap, const __grid_constant__ CUtensorMap xsmap,
                    const float *__restrict__ g, float *__restrict__ Y, int M, int N, int K,
                    int32_t *status) {
     extern __shared__ uint8_t smem_raw[];
@@ -251,11 +252,12 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ntm = (M + kBM - 1) / kBM, ntn = (N + kBN - 1) / kBN;
     const int ntiles = ntm * ntn, nk = K / (2 * kBKB);
-    const int64_t sf_row = K / 16;
 
     if (threadIdx.x == 0) {
         prefetch_tensor_map(&wmap);
         prefetch_tensor_map(&xmap);
+        prefetch_tensor_map(&wsmap);
+        prefetch_tensor_map(&xsmap);
         for (int s = 0; s < kNvStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -301,6 +303,8 @@ __global__ void __launch_bounds__(kNvThreads, 1)
                     uint8_t *st = smem + (size_t)s * kStageBytes;
                     tma_load_2d(st, &wmap, kk * kBKB, tm * kBM, &full[s]);
                     tma_load_2d(st + kTileBytes, &xmap, kk * kBKB, tn * kBN, &full[s]);
+                    tma_load_2d(st + 2 * kTileBytes, &wsmap, kk * 16, tm * kBM, &full[s]);
+                    tma_load_2d(st + 2 * kTileBytes + kSfTileBytes, &xsmap, kk * 16, tn * kBN, &full[s]);
                 }
             }
             // every copy in flight lands before the CTA may exit
@@ -346,24 +350,26 @@ __global__ void __launch_bounds__(kNvThreads, 1)
         // the tensor cores finish every issued MMA before the memory is freed
         if (gs > 0 && !mbar_wait(&empty[(gs - 1) % kNvStages], ((gs - 1) / kNvStages) & 1)) fail();
     } else if (warp < 6) {
-        // ---- scale warps: this warp's lane quadrant of every scale slot
+        // ---- scale warps: this warp's lane quadrant of every scale slot.  A
+        // stage's copies land only after the MMAs of the slot's previous
+        // round have completed (the producer waited for that), so the slot's
+        // tensor memory is free once the stage is full.
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         int gs = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-            const int tm = t % ntm, tn = t / ntm;
             for (int kk = 0; kk < nk; ++kk, ++gs) {
                 const int s = gs % kNvStages;
-                uint32_t va[16], vb[16];
-                load_stage_scales(wsf, M, (int64_t)tm * kBM, lane, sf_row, kk, va);
-                load_stage_scales(xsf, N, (int64_t)tn * kBN, lane, sf_row, kk, vb);
-                if (*abort_flag ||
-                    (gs >= kNvStages && !mbar_wait(&empty[s], ((gs / kNvStages) - 1) & 1))) {
+                if (*abort_flag || !mbar_wait(&full[s], (gs / kNvStages) & 1)) {
                     fail();
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                const uint8_t *st = smem + (size_t)s * kStageBytes + 2 * kTileBytes;
+                uint32_t va[16], vb[16];
+                stage_scales(st, lane, va);
+                stage_scales(st + kSfTileBytes, lane, vb);
                 const uint32_t col = tmem + lane_base + kSfCol0 + s * kSfColsPerStage;
                 tmem_st_16cols(col, va);
                 tmem_st_16cols(col + 16, vb);
@@ -387,13 +393,17 @@ __global__ void __launch_bounds__(kNvThreads, 1)
             const int m = tm * kBM + 32 * qe + lane;
 #pragma unroll 1
             for (int c = 0; c < kBN; c += 32) {
+                // 1/g of token c + lane of the chunk, broadcast per column
+                const int nl = tn * kBN + c + lane;
+                const float rg = nl < N ? __frcp_rn(__ldg(g + nl)) : 0.0f;
                 uint32_t r[32];
                 tmem_ld_32cols(tmem + ((uint32_t)(32 * qe) << 16) + b * kAccCols + c, r);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int n = tn * kBN + c + j;
-                    if (n < N && m < M) Y[(size_t)n * M + m] = __fdiv_rn(__uint_as_float(r[j]), __ldg(g + n));
+                    const float f = __shfl_sync(0xffffffffu, rg, j);
+                    if (n < N && m < M) Y[(size_t)n * M + m] = __uint_as_float(r[j]) * f;
                 }
             }
             tc_fence_before();
@@ -457,11 +467,16 @@ extern "C" rfp2_status rfp2_gemm_nvfp4(const uint8_t *Wnv, int64_t M, int64_t K,
     float *g = reinterpret_cast<float *>(xs + ((size_t)N * K / 16 + 255) / 256 * 256);
     nv_quant_kernel<<<(unsigned)N, kQThreads, 0, s>>>(X, (int)K, xc, xs, g);
     if (launch_status() != cudaSuccess) return RFP2_ECUDA;
-    CUtensorMap wmap, xmap;
+    const uint8_t *wsf = Wnv + (size_t)M * K / 2;
+    CUtensorMap wmap, xmap, wsmap, xsmap;
     if (!encode_tensor_map_2d(&wmap, Wnv, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)K / 2,
                               (uint64_t)M, (uint64_t)K / 2, kBKB, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tensor_map_2d(&xmap, xc, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)K / 2,
-                              (uint64_t)N, (uint64_t)K / 2, kBKB, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
+                              (uint64_t)N, (uint64_t)K / 2, kBKB, kBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_2d(&wsmap, wsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)K / 16,
+                              (uint64_t)M, (uint64_t)K / 16, 16, kBM) ||
+        !encode_tensor_map_2d(&xsmap, xs, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)K / 16,
+                              (uint64_t)N, (uint64_t)K / 16, 16, kBN))
         return RFP2_ECUDA;
     static std::mutex mu;
     static int configured[64] = {0};
@@ -476,8 +491,7 @@ extern "C" rfp2_status rfp2_gemm_nvfp4(const uint8_t *Wnv, int64_t M, int64_t K,
     const int64_t ntiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
     const int sms = sm_count(dev);
     const int grid = (int)(ntiles < sms ? ntiles : sms);
-    const uint8_t *wsf = Wnv + (size_t)M * K / 2;
     return from_cuda(launch(nv_gemm_kernel, dim3(grid), dim3(kNvThreads), kNvSmem, s, true, wmap,
-                            xmap, wsf, static_cast<const uint8_t *>(xs),
-                            static_cast<const float *>(g), Y, (int)M, (int)N, (int)K, dev_status));
+                            xmap, wsmap, xsmap, static_cast<const float *>(g), Y, (int)M, (int)N,
+                            (int)K, dev_status));
 }
