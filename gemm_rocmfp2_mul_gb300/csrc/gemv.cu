@@ -48,16 +48,17 @@ namespace rfp2 {
 namespace {
 
 // Launch shapes: two CTAs per SM; CW consumer warps + 1 producer warp, each
-// consumer decoding kRows rows of a stage at once.  One column: 16 warps of
-// at most 56 registers, four per SM sub-partition to hide each other's
-// latencies.  From two columns the extra activation and accumulator
-// registers would spill at 56, so 8 warps of up to 112 registers.
+// consumer decoding kRows rows of a stage at once.  Up to three columns: 16
+// warps of at most 56 registers, four per SM sub-partition to hide each
+// other's latencies (three columns spill a few registers and still gain,
+// measured).  From four columns the extra activation and accumulator
+// registers would spill heavily at 56, so 8 warps of up to 112 registers.
 #ifndef RFP2_GEMV_WIDE_CW
 #define RFP2_GEMV_WIDE_CW 8
 #endif
 template <int NC>
 constexpr int cw_of() {
-    return NC == 1 ? 16 : RFP2_GEMV_WIDE_CW;
+    return NC <= 3 ? 16 : RFP2_GEMV_WIDE_CW;
 }
 constexpr int kRows = 2;
 // Values (rows x columns) a warp reduces per stage, padded to a power of two.
@@ -565,7 +566,7 @@ struct Plan {
 
 size_t align16(size_t v) { return (v + 15) / 16 * 16; }
 
-int cw_for(int NC) { return NC == 1 ? cw_of<1>() : cw_of<2>(); }
+int cw_for(int NC) { return NC <= 3 ? cw_of<1>() : cw_of<4>(); }
 
 // K-slices of a row (a power of two) when each lane takes bpt blocks.
 int k_slices(int64_t KB, int bpt) {
