@@ -110,6 +110,44 @@ RFP2_DEV uint32_t e2m1_mag(float v) {
     return r & 0x7u;
 }
 
+// bf16 bits of 16 consecutive values -> fp32.
+RFP2_DEV void load_block16(const uint16_t *p, float (&f)[16]) {
+    const uint4 v0 = *reinterpret_cast<const uint4 *>(p);
+    const uint4 v1 = *reinterpret_cast<const uint4 *>(p + 8);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// One 16-value block with the row factor g: scale byte and 16 codes.
+RFP2_DEV void quant_block16(const float (&f)[16], float g, uint8_t *codes, uint8_t *sbyte) {
+    float bmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(f[i]));
+    const float t = __fmul_rn(__fdiv_rn(bmax, 6.0f), g);
+    const uint32_t b = e4m3_rn_sat(t);
+    const float s = e4m3_value(b);
+    uint32_t out[2] = {0u, 0u};
+    if (s != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float e = __fdiv_rn(__fmul_rn(f[i], g), s);
+            const uint32_t c = e2m1_mag(e) | (signbit(e) ? 8u : 0u);
+            out[i / 8] |= c << (4 * (i % 8));
+        }
+    }
+    *reinterpret_cast<uint2 *>(codes) = make_uint2(out[0], out[1]);
+    *sbyte = (uint8_t)b;
+}
+
+// The first kQCache blocks of a thread stay in registers between the amax
+// pass and the quantization (a row of K <= 16 * kQThreads * kQCache values is
+// read once); blocks beyond them are read again.
+constexpr int kQCache = 2;
+
 __global__ void __launch_bounds__(kQThreads) nv_quant_kernel(const uint16_t *__restrict__ X, int K,
                                                              uint8_t *__restrict__ codes,
                                                              uint8_t *__restrict__ sbytes,
@@ -119,16 +157,23 @@ __global__ void __launch_bounds__(kQThreads) nv_quant_kernel(const uint16_t *__r
     pdl_wait();
     const int64_t n = blockIdx.x;
     const uint16_t *x = X + n * K;
-    // amax of the row
+    const int nb = K / 16;
+    float f[kQCache][16];
     float m = 0.0f;
-    for (int k = threadIdx.x * 8; k < K; k += kQThreads * 8) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(x + k);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            m = fmaxf(m, fabsf(__uint_as_float(w[j] << 16)));
-            m = fmaxf(m, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
+    for (int c = 0; c < kQCache; ++c) {
+        const int j = threadIdx.x + c * kQThreads;
+        if (j < nb) {
+            load_block16(x + j * 16, f[c]);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(f[c][i]));
         }
+    }
+    for (int j = threadIdx.x + kQCache * kQThreads; j < nb; j += kQThreads) {
+        float t[16];
+        load_block16(x + j * 16, t);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(t[i]));
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -139,34 +184,15 @@ __global__ void __launch_bounds__(kQThreads) nv_quant_kernel(const uint16_t *__r
     for (int i = 1; i < kQThreads / 32; ++i) amax = fmaxf(amax, red[i]);
     const float g = amax > 0.0f ? __fdiv_rn(2688.0f, amax) : 1.0f;
     if (threadIdx.x == 0) g_out[n] = g;
-    // one 16-value block per thread per pass
-    for (int j = threadIdx.x; j < K / 16; j += kQThreads) {
-        const uint4 v0 = *reinterpret_cast<const uint4 *>(x + j * 16);
-        const uint4 v1 = *reinterpret_cast<const uint4 *>(x + j * 16 + 8);
-        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        float f[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            f[2 * i] = __uint_as_float(w[i] << 16);
-            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-        }
-        float bmax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(f[i]));
-        const float t = __fmul_rn(__fdiv_rn(bmax, 6.0f), g);
-        const uint32_t b = e4m3_rn_sat(t);
-        const float s = e4m3_value(b);
-        uint32_t out[2] = {0u, 0u};
-        if (s != 0.0f) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float e = __fdiv_rn(__fmul_rn(f[i], g), s);
-                const uint32_t c = e2m1_mag(e) | (signbit(e) ? 8u : 0u);
-                out[i / 8] |= c << (4 * (i % 8));
-            }
-        }
-        *reinterpret_cast<uint2 *>(codes + n * (K / 2) + j * 8) = make_uint2(out[0], out[1]);
-        sbytes[n * (K / 16) + j] = (uint8_t)b;
+    for (int c = 0; c < kQCache; ++c) {
+        const int j = threadIdx.x + c * kQThreads;
+        if (j < nb) quant_block16(f[c], g, codes + n * (K / 2) + j * 8, sbytes + n * (K / 16) + j);
+    }
+    for (int j = threadIdx.x + kQCache * kQThreads; j < nb; j += kQThreads) {
+        float t[16];
+        load_block16(x + j * 16, t);
+        quant_block16(t, g, codes + n * (K / 2) + j * 8, sbytes + n * (K / 16) + j);
     }
 }
 
