@@ -162,3 +162,40 @@ def test_gemm_full_config_sampled(g):
     ref = rows_parallel(lambda r: oracle.nvfp4_gemm(owc, ows, rows.size, K, xc, xs, rg, rows=r).T, sel).T
     err = rel_err_rows(Y[:, rows], ref)
     assert np.all(err <= TOL), err.max()
+
+
+def test_gemm_single_token_and_zero_weights(g):
+    """N = 1 (a 128-token tile with 127 zero-filled rows) and an all-zero
+    weight row (scale byte 0, codes +-0.5 times 0) give exact zeros there."""
+    M, K = 256, 1024
+    W = normal_weights(child_rngs(5, 1)[0], M, K, 0.02)
+    W[3] = 0.0
+    P = oracle.rfp2_pack(W)
+    X = float32_to_bf16_bits(np.random.default_rng(9).standard_normal((1, K)).astype(np.float32))
+    Y, img, ws = run(g, P, M, K, X)
+    xc, xs, gg = oracle.nvfp4_quant_act(bf16_to_f32(X))
+    wc, wsb = oracle.rfp2_to_nvfp4(P, M, K)
+    ref = oracle.nvfp4_gemm(wc, wsb, M, K, xc, xs, gg)
+    assert np.all(rel_err_rows(Y, ref) <= TOL)
+    assert Y[0, 3] == 0.0
+
+
+def test_error_codes(g):
+    import ctypes as C
+    import torch
+    L = g.lib()
+    OK, EINVAL, ESHAPE, EALIGN, EUNSUPPORTED, EWORKSPACE = 0, 1, 2, 3, 4, 9
+    p = C.c_void_p
+    buf = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    b = p(buf.data_ptr())
+    s = p(torch.cuda.current_stream().cuda_stream)
+    assert L.rfp2_to_nvfp4(None, 4, 64, b, s) == EINVAL
+    assert L.rfp2_to_nvfp4(b, 4, 40, b, s) == ESHAPE
+    assert L.rfp2_to_nvfp4(b, 4, 64, p(buf.data_ptr() + 8), s) == EALIGN
+    assert L.rfp2_nvfp4_weight_bytes(4, 64) == 4 * 32 + 4 * 4
+    assert L.rfp2_gemm_nvfp4(None, 128, 256, b, 1, b, b, 1 << 20, None, s) == EINVAL
+    assert L.rfp2_gemm_nvfp4(b, 128, 256, b, 0, b, b, 1 << 20, None, s) == ESHAPE
+    assert L.rfp2_gemm_nvfp4(b, 128, 384, b, 1, b, b, 1 << 20, None, s) == EUNSUPPORTED
+    assert L.rfp2_gemm_nvfp4(b, 128, 256, b, 1, b, b, 16, None, s) == EWORKSPACE
+    assert L.rfp2_gemm_nvfp4(b, 128, 256, p(buf.data_ptr() + 8), 1, b, b, 1 << 20, None, s) == EALIGN
+    torch.cuda.synchronize()
