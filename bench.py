@@ -676,45 +676,54 @@ def run_only(args):
     print(json.dumps(out), flush=True)
 
 
-def run_e2e(torch, gl, w, Pc, copies, steps):
+def run_e2e(torch, gl, w, Pc, copies, steps, C=16):
     """Same metric through the public API with the activations in pinned host
     memory: each step copies its x H2D, runs rfp2_gemv and copies its y D2H.
-    Steps alternate between two device buffers, and copies run on their own
-    streams (ordered by events), so one step's copies overlap the
-    neighbouring steps' GEMVs, as in a serving loop with independent
-    requests."""
-    x_h = [torch.from_numpy(w["x"][:1].copy()).pin_memory() for _ in range(2)]
-    y_h = [torch.empty((1, M_DEC), dtype=torch.float32).pin_memory() for _ in range(2)]
-    x_d = [torch.empty((1, K_DEC), dtype=torch.float32, device="cuda") for _ in range(2)]
-    y_d = [torch.empty((1, M_DEC), dtype=torch.float32, device="cuda") for _ in range(2)]
+    Steps go in chunks of C: the C input copies of a chunk (their own device
+    buffers) on one stream, one event, the chunk's C GEMVs back to back on
+    the compute stream, one event, the C output copies on a third stream.
+    Two sets of buffers let one chunk's copies overlap the neighbouring
+    chunks' GEMVs, as in a serving loop taking independent requests C at a
+    time.  Only the first GEMV of a chunk waits for an event; the others keep
+    the programmatic overlap with the GEMV before them.  Measured per step:
+    an event wait before every GEMV (two or eight buffers) 12.3 us; chunks of
+    8 / 16 / 32 steps 7.8 / 7.3 / 7.2 us."""
+    NB = 2 * C
+    x_h = [torch.from_numpy(w["x"][:1].copy()).pin_memory() for _ in range(NB)]
+    y_h = [torch.empty((1, M_DEC), dtype=torch.float32).pin_memory() for _ in range(NB)]
+    x_d = [torch.empty((1, K_DEC), dtype=torch.float32, device="cuda") for _ in range(NB)]
+    y_d = [torch.empty((1, M_DEC), dtype=torch.float32, device="cuda") for _ in range(NB)]
     ws = [torch.empty(gl.rfp2_gemv_workspace_bytes(1, K_DEC), dtype=torch.uint8, device="cuda")
-          for _ in range(2)]
+          for _ in range(NB)]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
     def steps_graph(n):
         s_comp = torch.cuda.current_stream()
         ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
-        started = [False, False]
-        for i in range(n):
-            b = i % 2
-            s_in.wait_stream(s_comp) if not started[b] else s_in.wait_event(ev["comp"][b])
+        for j in range(n // C):
+            h = j % 2
+            bufs = range(h * C, h * C + C)
+            # the chunk's buffers were last read by chunk j - 2's GEMVs
+            s_in.wait_stream(s_comp) if j < 2 else s_in.wait_event(ev["comp"][h])
             with torch.cuda.stream(s_in):
-                x_d[b].copy_(x_h[b], non_blocking=True)
-                ev["in"][b].record(s_in)
-            s_comp.wait_event(ev["in"][b])
-            if started[b]:
-                s_comp.wait_event(ev["out"][b])
-            gl.rfp2_gemv(Pc[i % copies], M_DEC, K_DEC, x_d[b], y=y_d[b], workspace=ws[b])
-            ev["comp"][b].record(s_comp)
-            s_out.wait_event(ev["comp"][b])
+                for b in bufs:
+                    x_d[b].copy_(x_h[b], non_blocking=True)
+                ev["in"][h].record(s_in)
+            s_comp.wait_event(ev["in"][h])
+            if j >= 2:
+                s_comp.wait_event(ev["out"][h])  # chunk j - 2's outputs copied out
+            for k, b in enumerate(bufs):
+                gl.rfp2_gemv(Pc[(j * C + k) % copies], M_DEC, K_DEC, x_d[b], y=y_d[b], workspace=ws[b])
+            ev["comp"][h].record(s_comp)
+            s_out.wait_event(ev["comp"][h])
             with torch.cuda.stream(s_out):
-                y_h[b].copy_(y_d[b], non_blocking=True)
-                ev["out"][b].record(s_out)
-            started[b] = True
+                for b in bufs:
+                    y_h[b].copy_(y_d[b], non_blocking=True)
+                ev["out"][h].record(s_out)
         s_comp.wait_stream(s_in)
         s_comp.wait_stream(s_out)
 
-    G = min(steps, 1000)
+    G = max(C, min(steps, 1000) // C * C)
     stream = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
@@ -738,7 +747,8 @@ def run_e2e(torch, gl, w, Pc, copies, steps):
     return {"value": round(WEIGHT_BYTES / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": 1 * K_DEC * 4, "d2h_bytes_per_step": 1 * M_DEC * 4,
             "us_per_step": round(ms * 1e3, 3),
-            "pipelining": "two buffers; H2D, GEMV and D2H on three streams ordered by events"}
+            "pipelining": f"chunks of {C} steps, {NB} buffers; H2D, GEMV and D2H on three "
+                          f"streams ordered by one event per chunk and stream"}
 
 
 # ---------------------------------------------------------------------------
