@@ -30,10 +30,12 @@
 //    word per lane and half-block at an offset that is a compile-time
 //    constant from a per-lane base, so the decode loop reads them with
 //    conflict-free 16-byte loads and no address arithmetic.
-//  * After each stage a warp reduces its rows' lane partials across the warp
-//    (a transposing butterfly over R*NC values) and stores them.  Rows split
-//    over several warps along K (very long rows) are combined through a
-//    double-buffered shared-memory slot guarded by mbarriers.
+//  * A warp reduces its rows' lane partials across the warp with a
+//    transposing butterfly and stores them: at one column after every three
+//    stages (the partials wait in registers, so the warp does not stall on
+//    the shuffle latency after each stage), else after every stage.  Rows
+//    split over several warps along K (very long rows) are combined through
+//    a double-buffered shared-memory slot guarded by mbarriers.
 //  * Every wait is an mbarrier wait with a time limit; a timeout stores
 //    RFP2_ETIMEOUT and the CTA winds down after its copies have landed.
 #include <mutex>
@@ -56,6 +58,9 @@ namespace {
 #ifndef RFP2_GEMV_WIDE_CW
 #define RFP2_GEMV_WIDE_CW 8
 #endif
+#ifndef RFP2_GEMV_DEFER
+#define RFP2_GEMV_DEFER 3
+#endif
 template <int NC>
 constexpr int cw_of() {
     return NC <= 3 ? 16 : RFP2_GEMV_WIDE_CW;
@@ -63,6 +68,14 @@ constexpr int cw_of() {
 constexpr int kRows = 2;
 // Values (rows x columns) a warp reduces per stage, padded to a power of two.
 constexpr int kVMax = 16;
+// Stages whose partials a warp keeps in registers before one reduction
+// covers them all (a warp owning whole rows; 1: reduce after every stage).
+// At one column the three stages a set decodes at the 14336 x 4096 decode
+// shape are reduced together.
+template <int NC>
+constexpr int defer_of() {
+    return NC == 1 ? RFP2_GEMV_DEFER : 1;
+}
 // Shared memory per CTA: two CTAs per SM, or one when a shape needs more.
 constexpr size_t kSmemPair = 113 * 1024;
 constexpr size_t kSmemOne = 227 * 1024;
@@ -119,6 +132,33 @@ RFP2_DEV float rcp_approx_f(float v) {
     return r;
 }
 
+// Scales from which the near-half rounding below is exact (every product and
+// residual in it stays a normal float).
+constexpr float kExactHalfMinD = 0x1p-100f;
+
+// roundf(fl(a / d)) for a value whose quotient estimate z (|z - a/d| <
+// 2^-14) lies within 2^-12 of a half-integer, for d >= kExactHalfMinD,
+// decided without a division.  With A = |a| and H = floor(|z|) + 1/2 that
+// half-integer, fl(A/d) >= H (roundf then goes away from zero) exactly when
+// A/d >= H - u/2, u being the float spacing just below H; at equality the
+// even significand would win (a tie there needs A to carry 25 significant
+// bits, so it never happens for float inputs; the test is kept all the same).
+// R = A - H*d is a small multiple of d's quantum (|R| < 2^-11 d, and H has
+// at most eight significant bits), so the FMA computes it exactly, and
+// (u/2)*d is exact too (u/2 is a power of two): one comparison decides.
+RFP2_DEV float round_quotient_near_half(float a, float d, float z) {
+    const float A = fabsf(a);
+    const float H = floorf(fabsf(z)) + 0.5f;
+    const float R = fmaf(-H, d, A);
+    const uint32_t hb = __float_as_uint(H);
+    // u/2: 2^(e-24) for H in (2^e, 2^(e+1)); 2^(e-25) when H = 2^e (H = 0.5)
+    const uint32_t drop = (hb & 0x7FFFFFu) == 0u ? 25u : 24u;
+    const float half_u = __uint_as_float(((hb >> 23) - drop) << 23);
+    const float t = half_u * d;
+    const bool up = R > -t || (R == -t && (hb & 1u) == 0u);
+    return copysignf((H - 0.5f) + (up ? 1.0f : 0.0f), a);
+}
+
 // Work split of the activation pass: a group is eight blocks of one column
 // that eight consecutive lanes l of one K-slice decode (same b), four
 // quantizing lanes per block and eight values per lane.  Group gi of a
@@ -147,8 +187,10 @@ RFP2_DEV ActSlot act_slot(int gi, int lane, int log_wk, int WK) {
 // comes from z = a * rcp.approx(d), whose relative error is below 2^-22, so
 // |z - a/d| < 2^-14 (|a/d| <= 127) and the IEEE quotient fl(a/d) lies within
 // 2^-17 of a/d.  Both therefore round to the same integer unless z is within
-// 2^-12 of a half-integer; lanes where it is (or where z is not finite: a
-// subnormal d whose reciprocal overflows) take the IEEE division and roundf.
+// 2^-12 of a half-integer; those values are rounded by an exact comparison
+// (round_quotient_near_half), or, where d is tiny (and z may not even be
+// finite: a subnormal d whose reciprocal overflows), by the IEEE division and
+// roundf.
 // Elsewhere z + 1.5*2^23 rounds z to that integer and holds it, in two's
 // complement, in the low byte of its bits.
 template <int NC, int BPT, int QP, int CW>
@@ -192,20 +234,50 @@ RFP2_DEV void quantize_to_smem(const float *__restrict__ x, bool vec, int K, int
             const float d = __fdiv_rn(m, 127.0f);
             const float rc = d != 0.0f ? rcp_approx_f(d) : 0.0f;
             uint32_t qb[8];
-            bool need = false;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float z = v[i][e] * rc;
-                const float zb = z + 12582912.0f;
-                const float t = z - (zb - 12582912.0f);
-                need |= !(fabsf(t) <= 0.5f - 0x1p-12f);
-                qb[e] = __float_as_uint(zb);
-            }
-            if (__any_sync(0xffffffffu, need) && need && d != 0.0f) {
+            if constexpr (NC == 1) {
+                // Every value also takes the exact near-half decision and
+                // keeps it where z is near a half-integer: no branch, so no
+                // warp waits on a division (every CTA waits for its slowest
+                // warp).  Only scales too small for that decision (never in
+                // practice) take the IEEE division.
+                const bool exact_half = d >= kExactHalfMinD;
+                uint32_t need = 0;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float qf = fminf(fmaxf(roundf(__fdiv_rn(v[i][e], d)), -127.0f), 127.0f);
-                    qb[e] = (uint32_t) static_cast<int>(qf);
+                    const float z = v[i][e] * rc;
+                    const float zb = z + 12582912.0f;
+                    const float t = z - (zb - 12582912.0f);
+                    const bool near = !(fabsf(t) <= 0.5f - 0x1p-12f);
+                    const float r = round_quotient_near_half(v[i][e], d, z);
+                    qb[e] = near && exact_half ? __float_as_uint(r + 12582912.0f) : __float_as_uint(zb);
+                    need |= (near && !exact_half ? 1u : 0u) << e;
+                }
+                if (__any_sync(0xffffffffu, need != 0u) && need != 0u && d != 0.0f) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float qf = fminf(fmaxf(roundf(__fdiv_rn(v[i][e], d)), -127.0f), 127.0f);
+                        if ((need >> e) & 1u) qb[e] = (uint32_t) static_cast<int>(qf);
+                    }
+                }
+            } else {
+                // several columns: the branch-free decision would cost more
+                // than it saves (measured), so the lanes with a value near a
+                // boundary take the IEEE division for all their values
+                bool need = false;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float z = v[i][e] * rc;
+                    const float zb = z + 12582912.0f;
+                    const float t = z - (zb - 12582912.0f);
+                    need |= !(fabsf(t) <= 0.5f - 0x1p-12f);
+                    qb[e] = __float_as_uint(zb);
+                }
+                if (__any_sync(0xffffffffu, need) && need && d != 0.0f) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float qf = fminf(fmaxf(roundf(__fdiv_rn(v[i][e], d)), -127.0f), 127.0f);
+                        qb[e] = (uint32_t) static_cast<int>(qf);
+                    }
                 }
             }
             if (!in[i]) continue;
@@ -449,8 +521,14 @@ __global__ void __launch_bounds__((cw_of<NC>() + 1) * 32, 2) gemv_stream_kernel(
                 if (*abort_flag) break;
                 issue(c, pol);
             }
-            // every copy in flight lands before the CTA may exit: wait for
-            // the latest round issued into each slot (of the first c stages)
+            // No copy may still be in flight when the CTA exits.  Without an
+            // abort every issued stage is waited for by its consumer set
+            // before the CTA can exit, so the producer leaves at once (a
+            // drain here was measured to hold the CTA up to ~0.8 us after
+            // its last consumer).  After an abort (a wait ran out; consumers
+            // may have left early) it waits for the latest round issued into
+            // each slot of the first c stages.
+            if (*abort_flag == 0) return;
             for (int s = 0; s < S; ++s) {
                 const int h = s % H, jj = s / H, sh = (S - h + H - 1) / H;
                 if (c <= h) continue;
@@ -463,9 +541,30 @@ __global__ void __launch_bounds__((cw_of<NC>() + 1) * 32, 2) gemv_stream_kernel(
         return;
     }
 
-    // ---- consumers: activations into shared memory, then the stages
+    // ---- consumers: the activations into shared memory, then the stages
     const int log_wk = __ffs(WK) - 1;
     constexpr int QP = act_groups_per_pass<NC, kCW>();
+    // The warp's place in the CTA.  At one column it is worked out before the
+    // dependency wait (it does not depend on the earlier work); with more
+    // columns the quantize needs those registers, so it comes after.
+    struct WarpPlace {
+        int set, rg, wk;
+        uint32_t row_off;
+    };
+    auto place_warp = [&]() {
+        WarpPlace w;
+        w.set = warp / G;
+        const int g = warp - w.set * G;
+        w.rg = g >> log_wk;
+        w.wk = g & (WK - 1);
+        const int kb = (w.wk * 32 + lane) * BPT;
+        // a row past the CTA's last one still lies inside the stage: it is
+        // computed from stale bytes and never stored
+        w.row_off = (uint32_t)(w.rg * kRows) * rowbytes + (kb < KB ? (uint32_t)kb * 10 : 0u);
+        return w;
+    };
+    WarpPlace wp;
+    if constexpr (NC == 1) wp = place_warp();
     pdl_wait();
     if constexpr (FQ) {
         quantize_to_smem<NC, BPT, QP, kCW>(a.x, a.x_vec != 0, a.K, WK, log_wk, warp, lane, actq,
@@ -483,28 +582,86 @@ __global__ void __launch_bounds__((cw_of<NC>() + 1) * 32, 2) gemv_stream_kernel(
         return;
     }
 
-    const int set = warp / G, g = warp - set * G;
-    const int rg = g >> log_wk, wk = g & (WK - 1);
+    if constexpr (NC != 1) wp = place_warp();
+    const int set = wp.set, rg = wp.rg, wk = wp.wk;
     const int wid = set * RGS + rg;  // row-group id, < kCW / WK
     const int kb0 = (wk * 32 + lane) * BPT;
     const bool active = kb0 < KB;
     const uint8_t *abase = actq + ((size_t)wk * BPT * 2 * NC * 32 + lane) * 16;
     const float *dbase = actd + (size_t)wk * BPT * NC * 32 + lane;
-    // a row past the CTA's last one still lies inside the stage: it is
-    // computed from stale bytes and never stored
-    const uint32_t row_off = (uint32_t)(rg * kRows) * rowbytes + (active ? (uint32_t)kb0 * 10 : 0u);
+    const uint32_t row_off = wp.row_off;
+    int slot = set, phase = 0;  // the set's own slots: set, set + H, ... < S
+
+    // the stage in `slot` is in shared memory (false: time limit or abort);
+    // the abort flag is read only when the stage has not landed yet
+    auto stage_ready = [&]() {
+        if (mbar_try_wait(&full[slot], phase)) return true;
+        if (*abort_flag || !mbar_wait(&full[slot], phase)) {
+            record_status(a.status, RFP2_ETIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+        return true;
+    };
+    auto next_slot = [&]() {
+        slot += H;
+        if (slot >= S) {
+            slot = set;
+            phase ^= 1;
+        }
+    };
+
+    constexpr int D = defer_of<NC>();
+    if (D > 1 && WK == 1) {
+        // A warp owns whole rows: the lane partials of D consecutive stages
+        // stay in registers and one transposing reduction covers them all,
+        // so the warp does not stall on the reduction's shuffle latency
+        // after every stage.
+        constexpr int VS = kRows * NC;
+        constexpr int VD = NextPow2<D * VS>::v;
+        constexpr int LD = Log2<VD>::v;
+        const int idx = lane >> (5 - LD);
+        const bool writer = (lane & ((32 >> LD) - 1)) == 0 && idx < D * VS;
+        const int vj = idx / VS, vr = (idx / NC) % kRows, vn = idx % NC;
+        for (int c0 = set; c0 < nstages; c0 += D * H) {
+            float part[D][kRows][NC];
+#pragma unroll
+            for (int j = 0; j < D; ++j)
+#pragma unroll
+                for (int r = 0; r < kRows; ++r)
+#pragma unroll
+                    for (int n = 0; n < NC; ++n) part[j][r][n] = 0.0f;
+#pragma unroll
+            for (int j = 0; j < D; ++j) {
+                if (c0 + j * H < nstages) {
+                    if (!stage_ready()) return;
+                    if (active)
+                        decode_rows<NC, BPT, kRows>(smem + (size_t)slot * stage_bytes + row_off,
+                                                    rowbytes, abase, dbase, part[j]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[slot]);
+                    next_slot();
+                }
+            }
+            float vals[VD];
+#pragma unroll
+            for (int i = 0; i < VD; ++i)
+                vals[i] = i < D * VS ? part[i / VS][(i / NC) % kRows][i % NC] : 0.0f;
+            const float total = warp_transpose_reduce<VD>(vals, lane);
+            const int c = c0 + vj * H;
+            const int row = c * SR + rg * kRows + vr;
+            if (writer && c < nstages && row < nrows) a.y[(int64_t)vn * a.M + r_begin + row] = total;
+        }
+        return;
+    }
+
     // this lane's value after the warp reduction: row vr, column vn
     const int idx = lane >> (5 - L);
     const bool writer = (lane & ((32 >> L) - 1)) == 0 && idx < kRows * NC;
     const int vr = idx / NC, vn = idx - vr * NC;
-    int slot = set, phase = 0;  // the set's own slots: set, set + H, ... < S
-    int it = 0;                 // stages this warp has done
+    int it = 0;  // stages this warp has done
     for (int c = set; c < nstages; c += H, ++it) {
-        if (*abort_flag || !mbar_wait(&full[slot], phase)) {
-            record_status(a.status, RFP2_ETIMEOUT);
-            *abort_flag = 1;
-            return;
-        }
+        if (!stage_ready()) return;
         float acc[kRows][NC];
 #pragma unroll
         for (int r = 0; r < kRows; ++r)
@@ -547,11 +704,7 @@ __global__ void __launch_bounds__((cw_of<NC>() + 1) * 32, 2) gemv_stream_kernel(
             }
         }
         if (store) a.y[(int64_t)vn * a.M + r_begin + row] = total;
-        slot += H;
-        if (slot >= S) {
-            slot = set;
-            phase ^= 1;
-        }
+        next_slot();
     }
 }
 

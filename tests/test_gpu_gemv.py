@@ -87,10 +87,13 @@ def test_quantize_bit_exact(g, kind, N, K):
 
 
 @pytest.mark.parametrize("kind", KINDS)
-@pytest.mark.parametrize("N,K", [(1, 4096), (2, 2048), (1, 256), (2, 16384)])
+@pytest.mark.parametrize("N,K", [(1, 4096), (2, 2048), (1, 256), (2, 16384), (3, 4096), (4, 1024),
+                                 (8, 512)])
 def test_gemv_quantize_bit_exact(g, kind, N, K):
-    """rfp2_gemv quantizes inside the GEMV kernel at batch <= 2; the q and d it
-    leaves in the workspace are the oracle's, bit for bit."""
+    """rfp2_gemv quantizes inside the GEMV kernel at batch <= 8; the q and d it
+    leaves in the workspace are the oracle's, bit for bit (the "ties" kind puts
+    a/d within a few ulps of half-integers, where the kernel decides the
+    rounding by an exact comparison instead of the division)."""
     import torch
     x = _inputs(kind, N, K, seed=7 * N + K)
     W = normal_weights(np.random.default_rng(K), 160, K, 0.02)
