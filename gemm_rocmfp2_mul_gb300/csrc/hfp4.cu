@@ -248,6 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bulk_g2s(bst + (size_t)s * bstage_bytes, a.frag + (int64_t)ks0 * a.N * 4, bbytes,
                              &full[s]);
             }
+            // no copy may be in flight when the CTA exits: without an abort
+            // every consumer warp waits for every chunk before it finishes,
+            // so only an aborted CTA waits here for its last copies
+            if (*abort_flag == 0) return;
             for (int i = max(0, c - S); i < c; ++i)
                 if (!mbar_wait(&full[i % S], (i / S) & 1)) record_status(a.status, RFP2_ETIMEOUT);
         }
