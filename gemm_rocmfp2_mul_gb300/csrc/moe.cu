@@ -48,6 +48,12 @@ constexpr int kGroupCols = RFP2_MOE_COLS;  // tokens per group (activation regis
 constexpr int kBpt = 2;                    // blocks per thread
 constexpr int kRows = RFP2_MOE_ROWS;       // rows per warp per chunk
 constexpr int kChunksPerTile = RFP2_MOE_CHUNKS_PER_TILE;  // rows per unit = chunks of RG*kRows
+// Chunks whose partials a consumer warp keeps in registers before one warp
+// reduction covers them (at most 16 values: kRows x tokens per chunk).
+template <int NC>
+constexpr int defer_chunks() {
+    return kRows * NC <= 4 ? 4 : kRows * NC <= 8 ? 2 : 1;
+}
 constexpr int kMaxPairs = 4096;
 constexpr int kRouteThreads = 1024;
 
@@ -227,6 +233,29 @@ struct MoeArgs {
     MoeWs ws;
 };
 
+// Consumer side, one warp per row (no K-slices): decode chunk c into the R x
+// NC lane partials `part` and release its stage at once; the reduction over
+// the warp is left to the caller.  Returns false when the CTA must stop.
+template <int NC, int BPT, int R>
+RFP2_DEV bool decode_chunk(Ring &r, int c, int wg, int lane, int kb0, bool active, int rowbytes,
+                           const Act<NC, BPT> &A, float (&part)[R][NC], int32_t *status) {
+    const int s = c % r.nstages;
+    if (!mbar_try_wait(&r.full[s], (c / r.nstages) & 1)) {
+        if (*r.abort_flag || !mbar_wait(&r.full[s], (c / r.nstages) & 1)) {
+            record_status(status, RFP2_ETIMEOUT);
+            *r.abort_flag = 1;
+            return false;
+        }
+    }
+    const uint8_t *base = r.stages + (size_t)s * r.chunk_bytes + (size_t)wg * R * rowbytes +
+                          (active ? kb0 * 10 : 0);
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) row_dot<NC, BPT>(base + rr * rowbytes, A, part[rr]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&r.empty[s]);
+    return true;
+}
+
 template <int NC>
 __device__ bool consume_group(Ring &r, const MoeArgs &a, int4 grp, int t_begin, int t_end, int &c,
                               int wg, int wk, int lane, int kb0, bool active, int rowbytes,
@@ -244,10 +273,64 @@ __device__ bool consume_group(Ring &r, const MoeArgs &a, int4 grp, int t_begin, 
         load_act<NC, kBpt, true>(A, q, d, a.K, kb0, active, cols);
     else
         load_act<NC, kBpt, false>(A, q, d, a.K, kb0, active, cols);
+    const int cr = r.RG * kRows;
+    constexpr int VS = kRows * NC;
+    constexpr int D = defer_chunks<NC>();
+    if (D > 1 && a.WK == 1) {
+        // A warp owns whole rows: the partials of D consecutive chunks stay
+        // in registers (each chunk's stage is released as soon as it is
+        // decoded) and one transposing reduction covers them, so the warps
+        // do not all stall on a shuffle chain after every chunk.
+        constexpr int VD = NextPow2<D * VS>::v;
+        constexpr int LD = Log2<VD>::v;
+        const int idx = lane >> (5 - LD);
+        const bool writer = (lane & ((32 >> LD) - 1)) == 0 && idx < D * VS;
+        const int vj = idx / VS, vr = (idx / NC) % kRows, vn = idx % NC;
+        float *yw = ycol[0];
+#pragma unroll
+        for (int n = 1; n < NC; ++n)
+            if (vn == n) yw = ycol[n];
+        int t = t_begin, ch = 0;
+        while (t < t_end) {
+            float part[D][kRows][NC];
+#pragma unroll
+            for (int j = 0; j < D; ++j)
+#pragma unroll
+                for (int rr = 0; rr < kRows; ++rr)
+#pragma unroll
+                    for (int n = 0; n < NC; ++n) part[j][rr][n] = 0.0f;
+            int wrow = 0, wlim = 0;  // the writer's row and its tile's end
+#pragma unroll
+            for (int j = 0; j < D; ++j) {
+                if (t < t_end) {
+                    const int r0 = t * a.tile_rows;
+                    const int r1 = min(a.M, r0 + a.tile_rows);
+                    if (j == vj) {
+                        wrow = r0 + ch * cr + wg * kRows + vr;
+                        wlim = r1;
+                    }
+                    if (!decode_chunk<NC, kBpt, kRows>(r, c, wg, lane, kb0, active, rowbytes, A,
+                                                       part[j], a.status))
+                        return false;
+                    ++c;
+                    if (++ch == (r1 - r0 + cr - 1) / cr) {
+                        ch = 0;
+                        ++t;
+                    }
+                }
+            }
+            float vals[VD];
+#pragma unroll
+            for (int i = 0; i < VD; ++i)
+                vals[i] = i < D * VS ? part[i / VS][(i / NC) % kRows][i % NC] : 0.0f;
+            const float total = warp_transpose_reduce<VD>(vals, lane);
+            if (writer && wrow < wlim) yw[wrow] = total;
+        }
+        return true;
+    }
     for (int t = t_begin; t < t_end; ++t) {
         const int r0 = t * a.tile_rows;
         const int r1 = min(a.M, r0 + a.tile_rows);
-        const int cr = r.RG * kRows;
         const int nch = (r1 - r0 + cr - 1) / cr;
         for (int ch = 0; ch < nch; ++ch, ++c) {
             int64_t rows[kRows];
