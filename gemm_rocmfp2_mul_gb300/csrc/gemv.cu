@@ -31,9 +31,10 @@
 //    constant from a per-lane base, so the decode loop reads them with
 //    conflict-free 16-byte loads and no address arithmetic.
 //  * A warp reduces its rows' lane partials across the warp with a
-//    transposing butterfly and stores them: at one column after every three
-//    stages (the partials wait in registers, so the warp does not stall on
-//    the shuffle latency after each stage), else after every stage.  Rows
+//    transposing butterfly and stores them: after every three stages at one
+//    column and every two at two columns (the partials wait in registers, so
+//    the warp does not stall on the shuffle latency after each stage), else
+//    after every stage.  Rows
 //    split over several warps along K (very long rows) are combined through
 //    a double-buffered shared-memory slot guarded by mbarriers.
 //  * Every wait is an mbarrier wait with a time limit; a timeout stores
@@ -71,10 +72,11 @@ constexpr int kVMax = 16;
 // Stages whose partials a warp keeps in registers before one reduction
 // covers them all (a warp owning whole rows; 1: reduce after every stage).
 // At one column the three stages a set decodes at the 14336 x 4096 decode
-// shape are reduced together.
+// shape are reduced together, at two columns pairs of stages; from three
+// columns the partials would spill.
 template <int NC>
 constexpr int defer_of() {
-    return NC == 1 ? RFP2_GEMV_DEFER : 1;
+    return NC == 1 ? RFP2_GEMV_DEFER : NC == 2 ? 2 : 1;
 }
 // Shared memory per CTA: two CTAs per SM, or one when a shape needs more.
 constexpr size_t kSmemPair = 113 * 1024;
