@@ -676,7 +676,7 @@ def run_only(args):
     print(json.dumps(out), flush=True)
 
 
-def run_e2e(torch, gl, w, Pc, copies, steps, C=16):
+def run_e2e(torch, gl, w, Pc, copies, steps, C=32):
     """Same metric through the public API with the activations in pinned host
     memory: each step copies its x H2D, runs rfp2_gemv and copies its y D2H.
     Steps go in chunks of C: the C input copies of a chunk (their own device
@@ -685,9 +685,9 @@ def run_e2e(torch, gl, w, Pc, copies, steps, C=16):
     Two sets of buffers let one chunk's copies overlap the neighbouring
     chunks' GEMVs, as in a serving loop taking independent requests C at a
     time.  Only the first GEMV of a chunk waits for an event; the others keep
-    the programmatic overlap with the GEMV before them.  Measured per step:
-    an event wait before every GEMV (two or eight buffers) 12.3 us; chunks of
-    8 / 16 / 32 steps 7.8 / 7.3 / 7.2 us."""
+    the programmatic overlap with the GEMV before them.  Measured per step
+    with the GEMV at 6.4 us a call: an event wait before every GEMV (two or
+    eight buffers) 12.3 us; chunks of 8 / 16 / 32 steps 7.8 / 7.3 / 7.2 us."""
     NB = 2 * C
     x_h = [torch.from_numpy(w["x"][:1].copy()).pin_memory() for _ in range(NB)]
     y_h = [torch.empty((1, M_DEC), dtype=torch.float32).pin_memory() for _ in range(NB)]
