@@ -58,6 +58,18 @@ def _inputs(kind, N, K, seed=0):
         x = np.nextafter(x, np.where(ulps > 0, np.inf, -np.inf).astype(np.float32)) * (ulps != 0) + x * (ulps == 0)
         x[:, :, 0] = 127.0 * d[:, :, 0]
         x = x.reshape(N, K)
+    elif kind == "near_half":
+        # a within 16 float steps of (k + 1/2) * d0 for scales over 120
+        # binades, block max 127 * d0: exercises the kernel's exact
+        # near-half rounding on both sides of every boundary
+        d0 = (rng.uniform(1, 2, (N, K // 32, 1)) * np.exp2(rng.integers(-60, 60, (N, K // 32, 1))))
+        d0 = d0.astype(np.float32)
+        k = rng.integers(-127, 127, (N, K // 32, 32)).astype(np.float32) + np.float32(0.5)
+        x = (k * d0).astype(np.float32)
+        step = rng.integers(-16, 17, x.shape).astype(np.int32)
+        x = (x.view(np.int32) + step).view(np.float32)
+        x[:, :, 0] = np.float32(127) * d0[:, :, 0]
+        x = x.reshape(N, K)
     elif kind == "subnormal":
         # block maxima near and below the smallest normal: d is subnormal
         x = rng.normal(0, 1, (N, K)) * 10.0 ** rng.integers(-44, -36, (N, K // 32, 1)).repeat(32, 2).reshape(N, K)
@@ -73,7 +85,7 @@ def _inputs(kind, N, K, seed=0):
 
 # -- activation quantization ------------------------------------------------------
 
-KINDS = ["normal", "student_t", "wide", "edge", "ties", "subnormal"]
+KINDS = ["normal", "student_t", "wide", "edge", "ties", "near_half", "subnormal"]
 
 
 @pytest.mark.parametrize("kind", KINDS)
